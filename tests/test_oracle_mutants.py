@@ -1,0 +1,75 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each one.
+
+Each mutant is an edited copy of the oracle's C source compiled into a temporary library
+(on the CPU; nothing here touches the product or a GPU).  The pins of
+test_oracle_visibility / test_oracle_rope / test_oracle_attn are then run against the
+mutant, and at least one of them must fail.  This shows the pins are not vacuous: a
+dropped term, a wrong sign, an off-by-one index or a wrong exponent would not go
+unnoticed.
+"""
+import pytest
+
+import oracle
+from tests import test_oracle_attn as TA
+from tests import test_oracle_rope as TR
+from tests import test_oracle_visibility as TV
+
+MUTANTS = {
+    "rope_sign": ("const double y0 = x0 * c - x1 * s;", "const double y0 = x0 * c + x1 * s;"),
+    "rope_freq": ("(2.0 * (double)k) / (double)d_rope", "((double)k) / (double)d_rope"),
+    "rope_pos_no_prefix": ("const double pos = (double)prefix_len[b] + (double)depth[r];",
+                           "const double pos = (double)depth[r];"),
+    "score_drops_rope": ("for (int r = 0; r < DR; ++r) dot += (double)qR[r] * (double)kr[r];",
+                         "(void)kr;"),
+    "score_no_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "mask_tree_bit_off_by_one": ("ok[j] = (j < P) ? 1 : vrow[j - P];",
+                                 "ok[j] = (j < P) ? 1 : vrow[(j - P + 1) % Q];"),
+    "mask_drops_last_prefix_key": ("ok[j] = (j < P) ? 1 : vrow[j - P];",
+                                   "ok[j] = (j + 1 < P) ? 1 : (j < P ? 0 : vrow[j - P]);"),
+    "mask_all_tree_visible": ("ok[j] = (j < P) ? 1 : vrow[j - P];", "ok[j] = 1;"),
+    "lse_without_max": ("lse[qrow] = m + log(l);", "lse[qrow] = log(l);"),
+    "no_normalisation": ("const double p = exp(s[j] - m) / l;",
+                         "const double p = exp(s[j] - m);"),
+    "vis_misses_self": ("int k = i, steps = 0;",
+                        "int k = i ? par[i] : 0, steps = i ? 1 : 0;"),
+    "vis_depth_off_by_one": ("depth[(int64_t)b * Q + i] = steps;",
+                             "depth[(int64_t)b * Q + i] = steps + 1;"),
+    "tree_slot_wrong": ("tvo_row(&c, b, (int64_t)prefix_len[b] + i)",
+                        "tvo_row(&c, b, (int64_t)prefix_len[b] + i - 1 + (i == 0))"),
+    "value_uses_kpe_row": ("const float* ck = c_kv + tvo_row(&c, b, j) * ckv_stride;",
+                           "const float* ck = c_kv + tvo_row(&c, b, j > 0 ? j - 1 : 0) * ckv_stride;"),
+}
+
+PINS = [
+    TV.test_brute_force_all_trees_q6, TV.test_chain_is_lower_triangular,
+    TV.test_star_sees_root_and_self,
+    TR.test_position_zero_is_identity, lambda: TR.test_matches_complex_multiplication(64),
+    TR.test_d2_is_plane_rotation, TR.test_pair0_rotates_by_position_radians_and_norm_kept,
+    TR.test_golden_worked_example,
+    lambda: TA.test_matches_sdpa_with_networkx_mask(True, "random"),
+    TA.test_chain_tree_is_causal_attention, TA.test_root_row_and_q1_are_single_query_decode,
+    TA.test_zero_query_is_mean_and_lse_is_log_count,
+    TA.test_dominant_score_selects_row_and_ones_give_one, TA.test_golden_worked_example,
+    TA.test_full_step_chain_equals_rope_then_causal_attention,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    src = oracle.source_text()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor not found for {name}"
+    path = oracle.compile_variant(src.replace(old, new), str(tmp_path / f"mut_{name}.so"))
+    failures = 0
+    with oracle.use_library(path):
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError):
+                failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
+
+
+def test_unmutated_oracle_passes_all_pins():
+    for pin in PINS:
+        pin()

@@ -1,0 +1,391 @@
+"""Benchmark of one tree-verify step (visibility -> RoPE(q) -> RoPE(k into cache) -> attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: B=32 sequences, H=64 heads, q_len=33 draft-tree nodes (chain/random
+mix), ragged prefixes U{4096..8192}, d_latent=512, d_rope=64, bf16 latent cache in
+shuffled 64-token pages (synthetic, seeded).  Prints one JSON line.
+
+Metric: algorithmic attention TFLOP/s of the whole step (visible (row, key) pairs only,
+2*(2*d_latent + d_rope) flops per pair and head), with HBM GB/s and the roofline
+fraction of the attention kernel beside it.  Inputs are resident in HBM when the timed
+region starts; between steps a 256 MB buffer is written so that every step starts with
+a cold L2; each step is timed with CUDA events on the launching stream.
+
+--impl reference times the float64 CPU oracle (the repository's own reference
+implementation of the same step) on a bounded sample of the workload per step.
+With --gpus N > 1 every rank runs an independent replica of the workload (the step has
+no cross-GPU exchange); value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(PEAKS_FALLBACK)
+    d["source"] = "fallback"
+    return d
+
+
+def work_of(inp: dict):
+    """Algorithmic flops and bytes of the attention call (visible pairs only)."""
+    B, H, Q, DL, DR = inp["B"], inp["H"], inp["Q"], inp["DL"], inp["DR"]
+    es = 2 if inp["kv_dtype"] == "bf16" else 4
+    P = inp["prefix_len"].astype(np.int64)
+    tree_pairs = 0
+    for b in range(B):
+        dep = np.zeros(Q, np.int64)
+        for i in range(1, Q):
+            dep[i] = dep[inp["parent"][b, i]] + 1
+        tree_pairs += int((dep + 1).sum())
+    pairs = int((P * Q).sum()) + tree_pairs
+    flops = 2.0 * (2 * DL + DR) * pairs * H
+    kv_rows = int((P + Q).sum())
+    byts = (kv_rows * (DL + DR) * es + B * Q * H * (DL + DR) * es + B * Q * H * (DL + 1) * 4
+            + B * Q * (4 + 8) + B * 4)
+    return flops, byts, pairs
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def kernel_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary, when
+    it was taken on the current kernel source (hash match); else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel_tag)
+    if not ent or ent.get("source_sha") != source_sha():
+        return None
+    return ent
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_04_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_baseline(inp, seqs, repeat=1):
+    import oracle
+    from speculative_decoding_tree_04_gb300 import synth  # noqa: F401
+    oracle.build()
+    t0 = time.perf_counter()
+    for _ in range(repeat):
+        oracle.tree_verify_step(inp, seqs=seqs)
+    dt = (time.perf_counter() - t0) / repeat
+    sub = dict(inp)
+    sub["B"] = len(seqs)
+    sub["parent"] = inp["parent"][seqs]
+    sub["prefix_len"] = inp["prefix_len"][seqs]
+    fl, by, _ = work_of(sub)
+    return dt, fl, by, oracle.max_threads()
+
+
+def run_reference(args, inp, rank, world):
+    from speculative_decoding_tree_04_gb300 import synth
+    if rank != 0:
+        return
+    seqs = synth.sample_sequences(inp, args.ref_seqs)
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        pass
+    times = []
+    fl = by = 0
+    threads = 1
+    for _ in range(args.steps):
+        dt, fl, by, threads = cpu_baseline(inp, seqs)
+        times.append(dt)
+    t = float(np.mean(times))
+    val = fl / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample": f"{len(seqs)} of {inp['B']} sequences"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"sequences {list(map(int, seqs))} of {args.workload}"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "tree-verify attn TFLOP/s and HBM GB/s per GB300, % of binding roofline"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cfg5_bf16")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tcgen05")
+    ap.add_argument("--ref-seqs", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from speculative_decoding_tree_04_gb300 import synth
+
+    rank, world, local = dist_env()
+    inp = synth.generate(args.workload)
+    if args.impl == "reference":
+        run_reference(args, inp, rank, world)
+        return
+
+    import torch
+    from speculative_decoding_tree_04_gb300 import build as tvbuild
+    from speculative_decoding_tree_04_gb300 import tv
+    from speculative_decoding_tree_04_gb300.step import VerifyStep, _dev_float
+
+    tvbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    step = VerifyStep(inp, device=dev, path=args.path)
+    path = step.chosen_path()
+    flops, byts, pairs = work_of(inp)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step.run()
+    barrier()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.add_(1.0)                     # cold L2 for every step (outside the events)
+        s0, a0, a1, s1 = ev[k]
+        s0.record(stream)
+        step.visibility()
+        step.rope_q()
+        step.rope_k()
+        a0.record(stream)
+        step.attention()
+        a1.record(stream)
+        s1.record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    step_ms = [s0.elapsed_time(s1) for s0, _, _, s1 in ev]
+    attn_ms = [a0.elapsed_time(a1) for _, a0, a1, _ in ev]
+    ms = float(np.sum(step_ms)) / args.steps
+    ams = float(np.sum(attn_ms)) / args.steps
+    if pg is not None:
+        t = torch.tensor([ms, ams], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, ams = float(t[0]), float(t[1])
+
+    # ---- end to end through the public calls, host buffers in pinned memory ----------
+    host = {k: _dev_float(inp, k, dev, pin=True) for k in
+            ("q_latent", "q_pe", "kpe_tree", "c_kv", "k_pe")}
+    import torch as _t
+    host_int = {"parent": _t.from_numpy(inp["parent"]).pin_memory(),
+                "prefix_len": _t.from_numpy(inp["prefix_len"]).pin_memory()}
+    if inp["page_table"] is not None:
+        host_int["page_table"] = _t.from_numpy(inp["page_table"]).pin_memory()
+    out_h = _t.empty(step.out.shape, dtype=_t.float32).pin_memory()
+    lse_h = _t.empty(step.lse.shape, dtype=_t.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_int.values()))
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    dst = {"q_latent": step.q_latent, "q_pe": step.q_pe_raw, "kpe_tree": step.kpe_tree,
+           "c_kv": step.c_kv, "k_pe": step.k_pe, "parent": step.parent,
+           "prefix_len": step.prefix_len, "page_table": step.page_table}
+
+    def e2e_once():
+        for k, t in list(host.items()) + list(host_int.items()):
+            dst[k].copy_(t, non_blocking=True)
+        step.run()
+        out_h.copy_(step.out, non_blocking=True)
+        lse_h.copy_(step.lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_once()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_once()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    if rank != 0:
+        pg.destroy_process_group() if pg is not None else None
+        return
+
+    peaks = load_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12 * world
+    attn_tflops = flops / (ams * 1e-3) / 1e12
+    attn_gbs = byts / (ams * 1e-3) / 1e9
+    kernel_tag = "attn_tc" if path == tv.PATH_TCGEN05 else "attn_simt"
+    trf = kernel_traffic(kernel_tag + ":" + args.workload)
+    if path == tv.PATH_TCGEN05 or inp["kv_dtype"] == "bf16":
+        roof = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
+                "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS bf16_tflops)"}
+    else:
+        props = torch.cuda.get_device_properties(dev)
+        mhz = (clk or {}).get("sm_max_mhz", 2070.0)
+        alu = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": attn_tflops, "peak": alu, "unit": "TFLOP/s",
+                "frac": attn_tflops / alu,
+                "peak_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {mhz} MHz"}
+    roof["traffic"] = None if trf is None else trf["dram_bytes_per_launch"]
+    roof["algorithmic_bytes"] = byts
+    roof["hbm_gbs_achieved"] = attn_gbs
+    roof["hbm_frac"] = attn_gbs / peaks["hbm_gbs"]
+    roof["kernel_ms"] = ams
+
+    cpu = None
+    if not args.no_cpu_baseline and world >= 1:
+        seqs = synth.sample_sequences(inp, args.ref_seqs)
+        dt, fl, by, thr = cpu_baseline(inp, seqs)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"full step (visibility, RoPE, attention) of sequences "
+                         f"{list(map(int, seqs))} of {args.workload}, {dt:.1f} s"}
+
+    launches = step.launches_per_step() * args.steps
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if inp["kv_dtype"] == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": args.workload, "B": inp["B"], "H": inp["H"], "q_len": inp["Q"],
+                   "d_latent": inp["DL"], "d_rope": inp["DR"],
+                   "prefix_len": f"U{{4096..8192}} drawn, mean {float(inp['prefix_len'].mean()):.0f}"
+                   if args.workload == "cfg5_bf16" else f"mean {float(inp['prefix_len'].mean()):.0f}",
+                   "paged": inp["page_table"] is not None, "path": ["auto", "simt", "tcgen05"][path],
+                   "l2": "256 MB buffer written between steps (cold L2); per-step CUDA events",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_gbs": attn_gbs,
+        "attn_ms": ams,
+        "roofline": roof,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed": t_wall,
+        "cpu_baseline": cpu,
+        "source_sha": source_sha(),
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

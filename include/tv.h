@@ -1,0 +1,202 @@
+/*
+ * tv.h -- C ABI of libtv: GB300 (sm_103a) tree-verify MLA-absorb attention for DDTree
+ * speculative decoding.
+ *
+ * The operations come from three web pages about a native DDTree engine:
+ *   [RoPE]   "Precision as Correctness: The Float64 RoPE Decision in a Custom CUDA
+ *             Inference Engine"
+ *   [VERIFY] "The Precision Imperative: Validating Numerical Accuracy in a Custom CUDA
+ *             Attention Kernel"
+ *   [GOLDEN] "The Golden Reference: A Pivotal Moment in Building a Native DDTree
+ *             Inference Engine"
+ *
+ * One verify step of a draft tree with q_len = Q nodes (node 0 is the root) over a
+ * sequence whose cache already holds prefix_len = P tokens is:
+ *   1. tv_build_visibility: parent array -> ancestor-or-self bitsets and depths;
+ *   2. tv_rope_neox: NeoX RoPE at position P + depth on the queries' rope part, and on the
+ *      draft tokens' k_pe rows, which it writes into cache slots P + node;
+ *   3. tv_verify_attn: for every (sequence, node, head), softmax attention in latent
+ *      space over the P prefix keys plus the node's ancestor-or-self tree keys, returning
+ *      the softmax-weighted sum of latent rows and the log-sum-exp of the scores.
+ *
+ * Conventions (every entry point):
+ *   - Tensor pointers are DEVICE pointers owned by the caller, unless stated otherwise.
+ *     The library allocates no device memory; scratch is a caller-provided workspace.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     The return value reports synchronous argument checks and launch errors only.
+ *   - Data-dependent errors found on the device (an invalid parent array, a prefix that
+ *     does not fit the cache geometry, a device wait that ran out) are stored as a
+ *     negative tv_status into *status, a caller-owned device int32.  The library never
+ *     clears it: set it to TV_OK before the first call and read it when convenient.
+ *     `status` may be NULL, in which case such errors are dropped silently.
+ *   - On a non-OK return, tv_last_error() (thread-local) describes the failure.
+ *   - Element strides are in ELEMENTS, not bytes.
+ */
+#ifndef TV_H_
+#define TV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TV_OK = 0,
+  TV_ERR_INVALID_ARG = -1,  /* a pointer, size or stride is invalid */
+  TV_ERR_INVALID_TREE = -2, /* parent[0] != -1 or parent[i] outside [0, i) */
+  TV_ERR_UNSUPPORTED = -3,  /* valid but outside what the library implements (Q > 64 ...) */
+  TV_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed (see tv_last_error) */
+  TV_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (device status only) */
+  TV_ERR_WORKSPACE = -6,    /* workspace missing or smaller than the size query asked for */
+  TV_ERR_BOUNDS = -7        /* prefix_len[b] + Q exceeds the cache geometry (device) */
+} tv_status;
+
+typedef enum { TV_F32 = 0, TV_BF16 = 1 } tv_dtype;
+
+/* Kernel family for tv_verify_attn.  AUTO picks by shape and dtype; the others force one
+ * family (used by tests to check both) and fail with TV_ERR_UNSUPPORTED when it cannot
+ * run the request. */
+typedef enum { TV_PATH_AUTO = 0, TV_PATH_SIMT = 1, TV_PATH_TCGEN05 = 2 } tv_path;
+
+/*
+ * Geometry of the latent KV cache.  Logical key j (0 <= j < prefix_len[b] + Q) of
+ * sequence b lives in cache row
+ *     page_table[b*max_pages + j/page_size]*page_size + j%page_size   (paged), or
+ *     b*kv_stride_b + j                                                (page_table NULL).
+ * The draft-tree token of node i occupies logical key prefix_len[b] + i.  ([GOLDEN]
+ * §"Recursive Refinement of the Decode Loop Design" works out the cache slots of the root
+ * and draft tokens without printing a formula; the reading taken here is that the tree
+ * tokens follow the prefix in node order.)  Paged caches need page_size == 64 on the
+ * tensor-core path.
+ */
+typedef struct {
+  const int32_t* page_table; /* device [B, max_pages] int32, or NULL for contiguous */
+  int32_t page_size;         /* tokens per page (paged layout) */
+  int32_t max_pages;         /* row stride of page_table, pages per sequence at most */
+  int64_t kv_stride_b;       /* contiguous layout: cache rows per sequence */
+} tv_cache_layout;
+
+/*
+ * tv_build_visibility -- ancestor-or-self bitsets of a draft tree.
+ *
+ * [VERIFY] §Context: the verify kernel applies a visibility mask that decides which tree
+ * tokens each query may attend to; [GOLDEN] §"Principled Abstraction": the step is M query
+ * tokens against the cache under an [M, kv_len] mask.  Each node sees its ancestors and
+ * itself.
+ *
+ * parent     : device [B, Q] int32, topologically ordered: parent[b*Q] == -1 and
+ *              0 <= parent[b*Q+i] < i for i > 0.
+ * anc        : device [B, Q] uint64 out; bit k of anc[b*Q+i] is set iff node k is node i or
+ *              one of its ancestors.
+ * depth      : device [B, Q] int32 out; parent steps from node i to the root.
+ * dense_mask : device [B, Q, Q] uint8 out, nullable; dense_mask[(b*Q+i)*Q+k] = bit k of
+ *              anc[b*Q+i].
+ * status     : see the conventions above.  A sequence with an invalid parent array gets
+ *              anc = 0, depth = -1 (and an all-zero mask row) and TV_ERR_INVALID_TREE.
+ * Returns TV_ERR_UNSUPPORTED for Q > 64 (one 64-bit word per node), TV_ERR_INVALID_ARG
+ * for B < 0, Q < 1 or a NULL parent/anc/depth with B > 0.
+ */
+int tv_build_visibility(const int32_t* parent, int B, int Q, uint64_t* anc, int32_t* depth,
+                        uint8_t* dense_mask, int32_t* status, void* stream);
+
+/*
+ * tv_rope_neox -- NeoX (rotate-half) rotary embedding with a float64 angle.
+ *
+ * [RoPE] §"The Message" and §"What Input Knowledge Is Required" (item 1): split the rope
+ * vector in half and rotate each pair (k, k + d_rope/2) by cos/sin of the angle;
+ * §"The Float64 Decision": the angle and the trigonometry run in double precision and the
+ * result is converted to float32 at the end.  Here the rotation itself is also done in
+ * double, so the float32 result carries one rounding; bf16 output rounds that float32
+ * value to nearest-even once more.
+ *
+ * For every (b, i, h), with pos = prefix_len[b] + depth[b*Q+i] and, for k < d_rope/2,
+ * inv_k = 1 / base^(2k/d_rope), a = pos * inv_k:
+ *     out[k]          = in[k] cos a - in[k + d/2] sin a
+ *     out[k + d/2]    = in[k + d/2] cos a + in[k] sin a
+ *
+ * in  : element (b, i, h, r) at in[(b*Q+i)*in_stride_row + h*in_stride_head + r].
+ * out : element (b, i, h, r) at out[row*out_stride_row + h*out_stride_head + r] where
+ *       row = b*Q+i when out_cache is NULL, else the cache row of logical key
+ *       prefix_len[b] + i under *out_cache (host struct; the draft tokens' k_pe rows are
+ *       rotated straight into their cache slots).  in == out with equal strides is
+ *       allowed (in place).
+ * in_dt / out_dt : TV_F32 or TV_BF16 each.
+ * prefix_len [B], depth [B, Q]: device int32 (depth from tv_build_visibility; a negative
+ *       depth -- an invalid tree -- leaves that row untouched).  With out_cache, rows whose
+ *       slot lies outside the geometry (negative prefix_len, a page index >= max_pages, a
+ *       negative page-table entry, or a slot >= kv_stride_b) are skipped.
+ * Returns TV_ERR_INVALID_ARG for odd or non-positive d_rope, n_heads < 1, or strides
+ * that make rows overlap.
+ */
+int tv_rope_neox(const void* in, tv_dtype in_dt, int64_t in_stride_row,
+                 int64_t in_stride_head, void* out, tv_dtype out_dt, int64_t out_stride_row,
+                 int64_t out_stride_head, const tv_cache_layout* out_cache, int B, int Q,
+                 int n_heads, int d_rope, const int32_t* prefix_len, const int32_t* depth,
+                 double base, void* stream);
+
+/*
+ * Arguments of tv_verify_attn (absorbed-MLA tree-verify attention).
+ *
+ * [VERIFY] §"Input Knowledge Required" and [GOLDEN] §"The Absorb Form of MLA": the key
+ * projection is folded into the query, so the score of query row (b, i, h) against key j
+ * is taken in latent space:
+ *     s_j = scale * ( q_latent[b,i,h,:] . c_kv[j,:]  +  q_pe[b,i,h,:] . k_pe[j,:] )
+ * over the visible keys V = { j < P_b } U { P_b + k : bit k of anc[b*Q+i] }, and
+ *     out[b,i,h,:] = sum_{j in V} softmax(s)_j * c_kv[j,:],   lse[b,i,h] = ln sum exp(s_j).
+ */
+typedef struct {
+  uint32_t struct_size;     /* sizeof(tv_attn_args): ABI check */
+  int32_t B, H, Q;          /* batch, heads, q_len (tree nodes, 1..64) */
+  int32_t d_latent, d_rope; /* d_latent % 8 == 0, d_rope % 8 == 0 (vector loads) */
+  float scale;              /* softmax scale */
+  tv_dtype q_dt, kv_dt;     /* (F32, F32) or (BF16, BF16) */
+  const void* q_latent;     /* [B, Q, H, d_latent] contiguous */
+  const void* q_pe;         /* [B, Q, H, d_rope] contiguous, RoPE already applied */
+  const void* c_kv;         /* cache rows, row r at c_kv + r*ckv_row_stride (16 B aligned) */
+  const void* k_pe;         /* cache rows, row r at k_pe + r*kpe_row_stride (16 B aligned) */
+  int64_t ckv_row_stride, kpe_row_stride; /* elements; rows 16-byte aligned */
+  tv_cache_layout cache;    /* where key j of sequence b lives */
+  const int32_t* prefix_len; /* device [B] int32, 0 <= prefix_len[b] <= max_prefix_len */
+  int32_t max_prefix_len;   /* host-side bound on prefix_len, sizes the launch */
+  const uint64_t* anc;      /* device [B, Q] from tv_build_visibility */
+  float* out;               /* device [B, Q, H, d_latent] float32 out */
+  float* lse;               /* device [B, Q, H] float32 out (natural log) */
+  int32_t* status;          /* device int32, nullable (see conventions) */
+  int32_t path;             /* tv_path; TV_PATH_AUTO normally */
+  int32_t num_splits;       /* 0 = automatic; else force this many KV splits */
+} tv_attn_args;
+
+/* Bytes of workspace tv_verify_attn needs for these arguments (0 if none).  The size
+ * depends on B, H, Q, d_latent, max_prefix_len, the path and num_splits only. */
+size_t tv_verify_attn_workspace_size(const tv_attn_args* a);
+
+/* The kernel family TV_PATH_AUTO resolves to for these arguments, or a negative
+ * tv_status if the arguments are invalid. */
+int tv_verify_attn_path(const tv_attn_args* a);
+
+/*
+ * tv_verify_attn -- run the attention.  workspace: device memory of at least
+ * tv_verify_attn_workspace_size(a) bytes, 256-byte aligned (NULL allowed when the size
+ * is 0); it is scratch and may be reused once the call's work on `stream` is done.
+ * Rows of a sequence whose prefix_len is negative or does not fit the cache geometry get
+ * out = 0, lse = -inf and TV_ERR_BOUNDS in *status.  Page-table entries of the pages that
+ * hold keys 0 .. prefix_len[b]+Q-1 must name valid cache pages (they are not checked).
+ */
+int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void* stream);
+
+/* Text for a tv_status code (static storage). */
+const char* tv_status_string(int code);
+
+/* Description of the last failure on this host thread ("" if none). */
+const char* tv_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int tv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TV_H_ */

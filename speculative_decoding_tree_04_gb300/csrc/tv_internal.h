@@ -1,0 +1,60 @@
+// tv_internal.h -- declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tv.h"
+
+namespace tv {
+
+// Cache geometry passed by value to kernels.
+struct CacheGeom {
+  const int32_t* page_table;  // [B, max_pages] or nullptr
+  int32_t page_size;
+  int32_t max_pages;
+  int64_t kv_stride_b;
+};
+
+// Row of the cache holding logical key j of sequence b.
+__host__ __device__ __forceinline__ int64_t cache_row(const CacheGeom& g, int b, int64_t j) {
+  if (g.page_table) {
+    const int32_t pg = g.page_table[(int64_t)b * g.max_pages + j / g.page_size];
+    return (int64_t)pg * g.page_size + j % g.page_size;
+  }
+  return (int64_t)b * g.kv_stride_b + j;
+}
+
+// Store a device-detected error into the caller's status word (first writer wins is not
+// guaranteed; any negative code marks the call as failed).
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicMin(status, code);
+}
+
+// Launchers (each defined next to its kernel).  Return cudaError_t of the launch.
+cudaError_t launch_visibility(const int32_t* parent, int B, int Q, uint64_t* anc,
+                              int32_t* depth, uint8_t* mask, int32_t* status,
+                              cudaStream_t st);
+
+cudaError_t launch_rope(const void* in, tv_dtype in_dt, int64_t isr, int64_t ish, void* out,
+                        tv_dtype out_dt, int64_t osr, int64_t osh, const CacheGeom* cache,
+                        int B, int Q, int NH, int D, const int32_t* prefix_len,
+                        const int32_t* depth, double base, cudaStream_t st);
+
+// Work decomposition of the SIMT attention path.
+struct SimtPlan {
+  int head_blocks;   // ceil(H / 32)
+  int splits;        // KV splits (1 = no combine)
+  int chunk;         // keys per split (multiple of 32)
+};
+SimtPlan simt_plan(const tv_attn_args* a, int sm_count);
+size_t simt_workspace(const tv_attn_args* a, const SimtPlan& p);
+bool simt_supported(const tv_attn_args* a);
+cudaError_t launch_attn_simt(const tv_attn_args* a, const SimtPlan& p, void* ws,
+                             cudaStream_t st);
+
+// Split-KV combine: partial (out_s, lse_s) for s < splits -> final out, lse.
+cudaError_t launch_combine(const float* ws_out, const float* ws_lse, int splits,
+                           int64_t rows, int DL, float* out, float* lse, cudaStream_t st);
+
+}  // namespace tv

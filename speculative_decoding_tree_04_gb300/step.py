@@ -1,0 +1,118 @@
+"""One tree-verify step on the GPU, composed from the library's three calls.
+
+``VerifyStep`` holds the device buffers of a step (draft-tree parents, prefix lengths,
+queries, the latent KV cache, outputs) and runs, on one CUDA stream:
+
+    tv_build_visibility(parent)                     -> anc, depth
+    tv_rope_neox(q_pe, in place, pos = P + depth)   -> rotated query rope part
+    tv_rope_neox(kpe_tree -> cache rows P + i)      -> rotated draft-token k_pe in cache
+    tv_verify_attn(...)                             -> out [B,Q,H,DL], lse [B,Q,H]
+
+This module moves bytes and issues calls; all arithmetic runs in libtv's kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import tv
+
+
+def _dev_float(inp: dict, key: str, device, pin=False):
+    if inp["kv_dtype"] == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(inp[key + "_bits"]).view(np.int16)).view(
+            torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(inp[key], np.float32))
+    if pin:
+        return t.pin_memory()
+    return t.to(device)
+
+
+class VerifyStep:
+    """Device-resident inputs/outputs of one verify step plus the call sequence."""
+
+    HOST_KEYS = ("parent", "prefix_len", "page_table", "q_latent", "q_pe", "kpe_tree",
+                 "c_kv", "k_pe")
+
+    def __init__(self, inp: dict, device="cuda", path=tv.PATH_AUTO, num_splits=0):
+        self.inp = inp
+        self.device = torch.device(device)
+        self.path = path
+        self.num_splits = num_splits
+        d = self.device
+        B, Q, H, DL = inp["B"], inp["Q"], inp["H"], inp["DL"]
+        self.B, self.Q, self.H, self.DL, self.DR = B, Q, H, DL, inp["DR"]
+        self.parent = torch.from_numpy(inp["parent"]).to(d)
+        self.prefix_len = torch.from_numpy(inp["prefix_len"]).to(d)
+        self.page_table = (None if inp["page_table"] is None
+                           else torch.from_numpy(inp["page_table"]).to(d))
+        self.q_latent = _dev_float(inp, "q_latent", d)
+        self.q_pe_raw = _dev_float(inp, "q_pe", d)
+        self.kpe_tree = _dev_float(inp, "kpe_tree", d)
+        self.c_kv = _dev_float(inp, "c_kv", d)
+        self.k_pe = _dev_float(inp, "k_pe", d)
+        self.q_pe = torch.zeros_like(self.q_pe_raw)
+        self.anc = torch.empty((B, Q), dtype=torch.int64, device=d)
+        self.depth = torch.empty((B, Q), dtype=torch.int32, device=d)
+        self.out = torch.empty((B, Q, H, DL), dtype=torch.float32, device=d)
+        self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=d)
+        self.status = torch.zeros(1, dtype=torch.int32, device=d)
+        self.max_prefix = int(inp["prefix_len"].max()) if B else 0
+        self.cache = tv.make_cache(self.page_table, inp["page_size"], inp["kv_stride_b"])
+        self.workspace = None
+        self._alloc_workspace()
+
+    def attn_args(self):
+        return tv.attn_args(self.q_latent, self.q_pe, self.c_kv, self.k_pe, self.prefix_len,
+                            self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
+                            self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
+                            self.status, self.path, self.num_splits)
+
+    def _alloc_workspace(self):
+        need = tv.workspace_size(self.attn_args())
+        self.workspace = (torch.empty(need, dtype=torch.uint8, device=self.device)
+                          if need > 0 else None)
+
+    def chosen_path(self) -> int:
+        return tv.chosen_path(self.attn_args())
+
+    # -- the four calls of one step ------------------------------------------------
+    def visibility(self, stream=None):
+        tv.build_visibility(self.parent, self.anc, self.depth, status=self.status,
+                            stream=stream)
+
+    def rope_q(self, stream=None):
+        tv.rope_neox(self.q_pe_raw, self.q_pe, self.prefix_len, self.depth,
+                     self.inp["rope_base"], stream=stream)
+
+    def rope_k(self, stream=None):
+        tv.rope_neox(self.kpe_tree, self.k_pe, self.prefix_len, self.depth,
+                     self.inp["rope_base"], cache=self.cache, stream=stream)
+
+    def attention(self, stream=None):
+        tv.verify_attn(self.q_latent, self.q_pe, self.c_kv, self.k_pe, self.prefix_len,
+                       self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
+                       self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
+                       self.status, self.path, self.num_splits, workspace=self.workspace,
+                       stream=stream)
+
+    def run(self, stream=None):
+        self.visibility(stream)
+        self.rope_q(stream)
+        self.rope_k(stream)
+        self.attention(stream)
+
+    def launches_per_step(self) -> int:
+        """Kernels one run() enqueues: visibility, 2 RoPE, attention (+ combine if split)."""
+        return 4 + (1 if self.workspace is not None else 0)
+
+    # -- results --------------------------------------------------------------------
+    def results(self):
+        torch.cuda.synchronize(self.device)
+        anc = self.anc.cpu().numpy().view(np.uint64)
+        return dict(anc=anc, depth=self.depth.cpu().numpy(),
+                    q_pe_rot=self.q_pe.float().cpu().numpy(),
+                    k_pe_cache=self.k_pe.float().cpu().numpy(),
+                    out=self.out.cpu().numpy(), lse=self.lse.cpu().numpy(),
+                    status=int(self.status.item()))

@@ -1,0 +1,242 @@
+"""Thin ctypes binding of libtv (the C ABI in include/tv.h), with the same call names.
+
+Only argument marshalling happens here: torch tensors supply device pointers, shapes,
+strides and the current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU fallback: if libtv.so has not been built, or a call fails,
+this module raises.
+
+    build_visibility(parent, anc, depth, dense_mask=None, status=None)
+    rope_neox(x, out, prefix_len, depth, base=10000.0, cache=None)
+    verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtv.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "tv.h")
+
+TV_OK, TV_ERR_INVALID_ARG, TV_ERR_INVALID_TREE, TV_ERR_UNSUPPORTED = 0, -1, -2, -3
+TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_ERR_WORKSPACE, TV_ERR_BOUNDS = -4, -5, -6, -7
+TV_F32, TV_BF16 = 0, 1
+PATH_AUTO, PATH_SIMT, PATH_TCGEN05 = 0, 1, 2
+
+
+class TVError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{msg} (status {code})")
+        self.status = code
+
+
+class CacheLayout(ctypes.Structure):
+    _fields_ = [("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32), ("kv_stride_b", ctypes.c_int64)]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Q", ctypes.c_int32),
+        ("d_latent", ctypes.c_int32), ("d_rope", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("q_dt", ctypes.c_int), ("kv_dt", ctypes.c_int),
+        ("q_latent", ctypes.c_void_p), ("q_pe", ctypes.c_void_p),
+        ("c_kv", ctypes.c_void_p), ("k_pe", ctypes.c_void_p),
+        ("ckv_row_stride", ctypes.c_int64), ("kpe_row_stride", ctypes.c_int64),
+        ("cache", CacheLayout),
+        ("prefix_len", ctypes.c_void_p),
+        ("max_prefix_len", ctypes.c_int32),
+        ("anc", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+        ("path", ctypes.c_int32),
+        ("num_splits", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load():
+    """Open libtv.so (built by speculative_decoding_tree_04_gb300.build); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libtv.so is not built ({LIB_PATH}); run "
+                           "`python -m speculative_decoding_tree_04_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.tv_build_visibility.argtypes = [P, i32, i32, P, P, P, P, P]
+    lib.tv_rope_neox.argtypes = [P, i32, i64, i64, P, i32, i64, i64, ctypes.POINTER(CacheLayout),
+                                 i32, i32, i32, i32, P, P, dbl, P]
+    lib.tv_verify_attn_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
+    lib.tv_verify_attn_workspace_size.restype = ctypes.c_size_t
+    lib.tv_verify_attn_path.argtypes = [ctypes.POINTER(AttnArgs)]
+    lib.tv_verify_attn.argtypes = [ctypes.POINTER(AttnArgs), P, ctypes.c_size_t, P]
+    lib.tv_status_string.argtypes = [i32]
+    lib.tv_status_string.restype = ctypes.c_char_p
+    lib.tv_last_error.restype = ctypes.c_char_p
+    lib.tv_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER):
+    """Names of the functions include/tv.h declares (for symbol checks)."""
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tv_\w+)\s*\(", text, re.M)))
+
+
+def _check(rc, what):
+    if rc != TV_OK:
+        lib = load()
+        raise TVError(rc, f"{what}: {lib.tv_last_error().decode()}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TV_F32
+    if t.dtype == torch.bfloat16:
+        return TV_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libtv takes CUDA tensors only")
+
+
+def build_visibility(parent, anc, depth, dense_mask=None, status=None, stream=None):
+    """parent [B,Q] int32 -> anc [B,Q] int64 (bit patterns of uint64), depth [B,Q] int32."""
+    _need_cuda(parent, anc, depth, dense_mask, status)
+    assert parent.dtype == torch.int32 and anc.dtype in (torch.int64, torch.uint64)
+    assert parent.is_contiguous() and anc.is_contiguous() and depth.is_contiguous()
+    B, Q = parent.shape
+    rc = load().tv_build_visibility(_ptr(parent), B, Q, _ptr(anc), _ptr(depth),
+                                    _ptr(dense_mask), _ptr(status), _stream(stream))
+    _check(rc, "tv_build_visibility")
+
+
+def make_cache(page_table=None, page_size=64, kv_stride_b=0) -> CacheLayout:
+    if page_table is not None:
+        _need_cuda(page_table)
+        assert page_table.dtype == torch.int32 and page_table.is_contiguous()
+        return CacheLayout(page_table.data_ptr(), page_size, page_table.shape[1], 0)
+    return CacheLayout(None, page_size, 0, kv_stride_b)
+
+
+def rope_neox(x, out, prefix_len, depth, base=10000.0, cache: CacheLayout | None = None,
+              stream=None):
+    """NeoX RoPE on x [B,Q,H,D] (or [B,Q,D] for one head) into out.
+
+    Without ``cache`` out has x's shape (in place allowed).  With ``cache`` out is a cache
+    array [rows, D] (row stride out.stride(0)) and row (b, i) goes to the cache slot of
+    logical key prefix_len[b] + i.
+    """
+    _need_cuda(x, out, prefix_len, depth)
+    x4 = x if x.dim() == 4 else x.unsqueeze(2)
+    B, Q, NH, D = x4.shape
+    if x4.stride(-1) != 1 or out.stride(-1) != 1:
+        raise ValueError("innermost dimension must be contiguous")
+    isr, ish = x4.stride(1), x4.stride(2)
+    if x4.stride(0) != Q * isr:
+        raise ValueError("x rows must be uniformly strided over (B, Q)")
+    if cache is None:
+        o4 = out if out.dim() == 4 else out.unsqueeze(2)
+        if o4.stride(0) != Q * o4.stride(1):
+            raise ValueError("out rows must be uniformly strided over (B, Q)")
+        osr, osh = o4.stride(1), o4.stride(2)
+        cp = None
+    else:
+        osr, osh = out.stride(0), D
+        cp = ctypes.byref(cache)
+    rc = load().tv_rope_neox(_ptr(x), _dt(x), isr, ish, _ptr(out), _dt(out), osr, osh, cp,
+                             B, Q, NH, D, _ptr(prefix_len), _ptr(depth), float(base),
+                             _stream(stream))
+    _check(rc, "tv_rope_neox")
+
+
+def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
+              page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
+              num_splits=0) -> AttnArgs:
+    _need_cuda(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, page_table, status)
+    B, Q, H, DL = q_latent.shape
+    DR = q_pe.shape[-1]
+    for t in (q_latent, q_pe, prefix_len, anc, out, lse):
+        if not t.is_contiguous():
+            raise ValueError("q_latent, q_pe, prefix_len, anc, out, lse must be contiguous")
+    if c_kv.stride(-1) != 1 or k_pe.stride(-1) != 1:
+        raise ValueError("cache rows must be contiguous")
+    a = AttnArgs()
+    a.struct_size = ctypes.sizeof(AttnArgs)
+    a.B, a.H, a.Q, a.d_latent, a.d_rope = B, H, Q, DL, DR
+    a.scale = float(scale)
+    a.q_dt, a.kv_dt = _dt(q_latent), _dt(c_kv)
+    a.q_latent, a.q_pe = q_latent.data_ptr(), q_pe.data_ptr()
+    a.c_kv, a.k_pe = c_kv.data_ptr(), k_pe.data_ptr()
+    a.ckv_row_stride, a.kpe_row_stride = c_kv.stride(0), k_pe.stride(0)
+    a.cache = make_cache(page_table, page_size, kv_stride_b)
+    a.prefix_len = prefix_len.data_ptr()
+    a.max_prefix_len = int(max_prefix_len)
+    a.anc = anc.data_ptr()
+    a.out, a.lse = out.data_ptr(), lse.data_ptr()
+    a.status = None if status is None else status.data_ptr()
+    a.path, a.num_splits = int(path), int(num_splits)
+    return a
+
+
+def workspace_size(a: AttnArgs) -> int:
+    return int(load().tv_verify_attn_workspace_size(ctypes.byref(a)))
+
+
+def chosen_path(a: AttnArgs) -> int:
+    rc = load().tv_verify_attn_path(ctypes.byref(a))
+    if rc < 0:
+        _check(rc, "tv_verify_attn_path")
+    return rc
+
+
+_ws_cache: dict = {}
+
+
+def verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
+                page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
+                num_splits=0, workspace=None, stream=None):
+    """Tree-verify attention; out [B,Q,H,DL] and lse [B,Q,H] (float32) are written.
+
+    ``workspace`` (a CUDA uint8 tensor) is allocated through torch and cached per device
+    when not given."""
+    a = attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale,
+                  max_prefix_len, page_table, page_size, kv_stride_b, status, path, num_splits)
+    need = workspace_size(a)
+    if workspace is None and need > 0:
+        key = q_latent.device
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=q_latent.device)
+            _ws_cache[key] = ws
+        workspace = ws
+    wptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().tv_verify_attn(ctypes.byref(a), wptr, wbytes, _stream(stream))
+    _check(rc, "tv_verify_attn")
+    return a

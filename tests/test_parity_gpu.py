@@ -1,0 +1,178 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Every test draws seeded synthetic inputs, runs the whole verify step on the GPU
+(visibility -> RoPE(q_pe) -> RoPE(tree k_pe into the cache) -> attention) and the same
+step in the oracle, and compares:
+  * anc bitsets and depths: bit-exact;
+  * RoPE outputs: within one unit in the last place of the storage format (device and
+    host double-precision cos/sin may differ in the last bit);
+  * attention out and lse: max_abs <= 1e-5 and max_rel <= 1e-2 (float32 caches),
+    max_abs <= 2e-2 (bf16 caches; the oracle is fed the same bf16 values).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_tree_04_gb300 import synth, tv
+from speculative_decoding_tree_04_gb300.step import VerifyStep
+from tests.compare import assert_close, ulp
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("tvlib")]
+
+
+def run_pair(inp, path=tv.PATH_AUTO, num_splits=0, seqs=None):
+    step = VerifyStep(inp, path=path, num_splits=num_splits)
+    step.run()
+    g = step.results()
+    o = oracle.tree_verify_step(inp, seqs=seqs)
+    return step, g, o
+
+
+def check_step(inp, g, o, seqs=None):
+    dt = inp["kv_dtype"]
+    sel = slice(None) if seqs is None else np.asarray(seqs)
+    assert g["status"] == 0, tv.load().tv_status_string(g["status"])
+    assert np.array_equal(g["anc"], o["anc"])
+    assert np.array_equal(g["depth"], o["depth"])
+    # RoPE: query rope part and the tree rows written into the cache
+    assert np.all(np.abs(g["q_pe_rot"] - o["q_pe_rot"]) <= ulp(o["q_pe_rot"], dt))
+    assert np.all(np.abs(g["k_pe_cache"] - o["k_pe_cache"]) <= ulp(o["k_pe_cache"], dt))
+    e_out = assert_close(g["out"][sel], o["out"][sel], dt, "out")
+    e_lse = assert_close(g["lse"][sel], o["lse"][sel], dt, "lse")
+    return e_out, e_lse
+
+
+SMALL = ["cfg1_fp32", "cfg2_fp32", "cfg3_fp32", "cfg3_bf16"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_workload_parity_simt(name, splits):
+    inp = synth.generate(name)
+    step, g, o = run_pair(inp, path=tv.PATH_SIMT, num_splits=splits)
+    e_out, e_lse = check_step(inp, g, o)
+    print(name, "splits", splits, "out", e_out, "lse", e_lse)
+
+
+def test_workload_parity_cfg4_auto():
+    inp = synth.generate("cfg4_bf16")
+    step, g, o = run_pair(inp)
+    print("cfg4 path", step.chosen_path(), check_step(inp, g, o))
+
+
+def test_workload_parity_cfg5_sampled():
+    inp = synth.generate("cfg5_bf16")
+    seqs = synth.sample_sequences(inp, 4)
+    step, g, o = run_pair(inp, seqs=seqs)
+    print("cfg5 path", step.chosen_path(), "seqs", seqs, check_step(inp, g, o, seqs=seqs))
+
+
+EDGE = [
+    # (description, generate kwargs)
+    ("q_len 1 (single-query decode)", dict(B=3, H=8, Q=1, DL=512, DR=64, prefix=(5, 300))),
+    ("prefix 0 (pure tree)", dict(B=2, H=8, Q=9, DL=512, DR=64, prefix=(0, 0))),
+    ("q_len 64 (bitset limit)", dict(B=2, H=4, Q=64, DL=64, DR=16, prefix=(3, 70))),
+    ("kv_len not a multiple of 64, ragged", dict(B=5, H=16, Q=7, DL=128, DR=32, prefix=(1, 200))),
+    ("mid-page prefix, paged", dict(B=3, H=16, Q=17, DL=512, DR=64, prefix=(100, 130), paged=True)),
+    ("chain trees", dict(B=2, H=8, Q=12, DL=64, DR=16, prefix=(9, 40), tree="chain")),
+    ("star trees", dict(B=2, H=8, Q=12, DL=64, DR=16, prefix=(9, 40), tree="star")),
+    ("33 heads (partial head group)", dict(B=1, H=33, Q=5, DL=512, DR=64, prefix=(60, 60))),
+]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("desc,kw", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_cases(desc, kw, dtype):
+    inp = synth.generate(seed=zlib.crc32(desc.encode()) % 1000, dtype=dtype, **kw)
+    step, g, o = run_pair(inp)
+    check_step(inp, g, o)
+
+
+def test_invalid_tree_sets_status_and_zeroes_that_sequence():
+    inp = synth.generate(B=3, H=8, Q=6, DL=64, DR=16, prefix=(4, 9), seed=3)
+    inp["parent"][1, 3] = 5  # parent must precede the node
+    step = VerifyStep(inp)
+    step.run()
+    g = step.results()
+    assert g["status"] == tv.TV_ERR_INVALID_TREE
+    assert np.all(g["anc"][1] == 0) and np.all(g["depth"][1] == -1)
+    good = [0, 2]
+    o = oracle.tree_verify_step(dict(inp, parent=inp["parent"][good].copy(),
+                                     prefix_len=inp["prefix_len"][good].copy(),
+                                     q_latent=inp["q_latent"][good], q_pe=inp["q_pe"][good],
+                                     kpe_tree=inp["kpe_tree"][good], B=2,
+                                     kv_stride_b=inp["kv_stride_b"],
+                                     c_kv=np.concatenate([inp["c_kv"][:inp["kv_stride_b"]],
+                                                          inp["c_kv"][2 * inp["kv_stride_b"]:]]),
+                                     k_pe=np.concatenate([inp["k_pe"][:inp["kv_stride_b"]],
+                                                          inp["k_pe"][2 * inp["kv_stride_b"]:]])))
+    assert_close(g["out"][good], o["out"], "fp32", "out")
+    assert_close(g["lse"][good], o["lse"], "fp32", "lse")
+    # the invalid sequence sees only its prefix (no tree key is visible)
+    assert np.all(np.isfinite(g["out"][1]))
+
+
+def test_prefix_beyond_bound_reports_bounds():
+    inp = synth.generate(B=2, H=8, Q=5, DL=64, DR=16, prefix=(10, 10), seed=4)
+    step = VerifyStep(inp)
+    step.max_prefix = 10
+    step.prefix_len[1] = 11  # larger than the declared bound
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == tv.TV_ERR_BOUNDS
+    assert torch.all(step.out[1] == 0)
+    assert torch.all(torch.isinf(step.lse[1]))
+
+
+def test_guard_bands_untouched():
+    inp = synth.generate("cfg1_fp32")
+    step = VerifyStep(inp)
+    B, Q, H, DL = step.B, step.Q, step.H, step.DL
+    canary = float.fromhex("0x1.5555p+100")
+    big = torch.full((B * Q * H * DL + 2048,), canary, device="cuda")
+    step.out = big[1024:1024 + B * Q * H * DL].view(B, Q, H, DL)
+    bigl = torch.full((B * Q * H + 2048,), canary, device="cuda")
+    step.lse = bigl[1024:1024 + B * Q * H].view(B, Q, H)
+    step.run()
+    torch.cuda.synchronize()
+    assert torch.all(big[:1024] == canary) and torch.all(big[-1024:] == canary)
+    assert torch.all(bigl[:1024] == canary) and torch.all(bigl[-1024:] == canary)
+
+
+def test_q65_unsupported_on_device_call():
+    inp = synth.generate(B=1, H=2, Q=8, DL=64, DR=16, prefix=(4, 4), seed=1)
+    step = VerifyStep(inp)
+    parent = torch.zeros((1, 65), dtype=torch.int32, device="cuda")
+    anc = torch.zeros((1, 65), dtype=torch.int64, device="cuda")
+    depth = torch.zeros((1, 65), dtype=torch.int32, device="cuda")
+    with pytest.raises(tv.TVError) as e:
+        tv.build_visibility(parent, anc, depth)
+    assert e.value.status == tv.TV_ERR_UNSUPPORTED
+
+
+def test_dense_mask_matches_oracle():
+    inp = synth.generate(B=4, H=1, Q=33, DL=64, DR=16, prefix=(1, 1), seed=8, tree="wide")
+    parent = torch.from_numpy(inp["parent"]).cuda()
+    anc = torch.empty((4, 33), dtype=torch.int64, device="cuda")
+    depth = torch.empty((4, 33), dtype=torch.int32, device="cuda")
+    mask = torch.empty((4, 33, 33), dtype=torch.uint8, device="cuda")
+    tv.build_visibility(parent, anc, depth, dense_mask=mask)
+    vis, dep, ancs = oracle.visibility(inp["parent"])
+    assert np.array_equal(mask.cpu().numpy(), vis)
+    assert np.array_equal(depth.cpu().numpy(), dep)
+
+
+def test_all_six_node_trees_bit_exact():
+    import itertools
+    trees = [np.array([-1, *c], np.int32) for c in itertools.product(*[range(i) for i in range(1, 6)])]
+    par = np.stack(trees)
+    parent = torch.from_numpy(par).cuda()
+    anc = torch.empty(par.shape, dtype=torch.int64, device="cuda")
+    depth = torch.empty(par.shape, dtype=torch.int32, device="cuda")
+    tv.build_visibility(parent, anc, depth)
+    vis, dep, ancs = oracle.visibility(par)
+    assert np.array_equal(anc.cpu().numpy().view(np.uint64), ancs)
+    assert np.array_equal(depth.cpu().numpy(), dep)

@@ -186,6 +186,35 @@ int tv_verify_attn_path(const tv_attn_args* a);
  */
 int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * tv_verify_attn_noalloc -- tv_verify_attn for callers that cannot allocate device memory.
+ *
+ * The pages describe nothing like this; it exists for callers that cannot give the library
+ * a workspace: a plugin inside a host program that owns all device memory and offers no
+ * allocator, a serving loop that must not call cudaMalloc/cudaFree because they can
+ * synchronise the device, or a caller whose device memory budget is fixed in advance.
+ *
+ * It runs the CUDA-core attention kernel (TV_PATH_AUTO or TV_PATH_SIMT; TV_PATH_TCGEN05
+ * is rejected) and keeps the split-KV partial results in a fixed array of
+ * TV_NOALLOC_SCRATCH_BYTES bytes that the library reserves in device memory on every GPU
+ * that loads it, held until the process exits.  It never allocates.  The caller still
+ * passes every input and output through `a`.
+ *   - The first call on a device looks up the array's address on that device (a
+ *     cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - A request whose scratch need (tv_verify_attn_workspace_size(a) for the CUDA-core
+ *     path) exceeds TV_NOALLOC_SCRATCH_BYTES returns TV_ERR_WORKSPACE with an explanation
+ *     in tv_last_error().
+ *   - All calls share the one array and it keeps the last call's contents (nothing in it
+ *     needs to start at zero).  Calls whose kernels can overlap on the GPU -- unordered
+ *     streams, several host threads -- race on it; the caller must serialise them.
+ * Results equal tv_verify_attn's on the CUDA-core path.
+ */
+#define TV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int tv_verify_attn_noalloc(const tv_attn_args* a, void* stream);
+
+/* Size in bytes of the fixed scratch array behind tv_verify_attn_noalloc. */
+size_t tv_noalloc_scratch_bytes(void);
+
 /* Text for a tv_status code (static storage). */
 const char* tv_status_string(int code);
 

@@ -84,6 +84,11 @@ int resolve_path(const tv_attn_args* a) {
 
 }  // namespace
 
+namespace tv {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+int current_sm_count() { return sm_count(); }
+}  // namespace tv
+
 extern "C" {
 
 int tv_version(void) { return 100; }

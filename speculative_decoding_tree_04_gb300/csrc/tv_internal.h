@@ -57,4 +57,10 @@ cudaError_t launch_attn_simt(const tv_attn_args* a, const SimtPlan& p, void* ws,
 cudaError_t launch_combine(const float* ws_out, const float* ws_lse, int splits,
                            int64_t rows, int DL, float* out, float* lse, cudaStream_t st);
 
+// Set the thread-local text returned by tv_last_error() (defined in tv_api.cu).
+void set_last_error(const char* msg);
+
+// Number of SMs of the current device (148 if it cannot be queried).
+int current_sm_count();
+
 }  // namespace tv

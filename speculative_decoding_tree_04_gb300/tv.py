@@ -79,6 +79,8 @@ def load():
     lib.tv_verify_attn_workspace_size.restype = ctypes.c_size_t
     lib.tv_verify_attn_path.argtypes = [ctypes.POINTER(AttnArgs)]
     lib.tv_verify_attn.argtypes = [ctypes.POINTER(AttnArgs), P, ctypes.c_size_t, P]
+    lib.tv_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), P]
+    lib.tv_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.tv_status_string.argtypes = [i32]
     lib.tv_status_string.restype = ctypes.c_char_p
     lib.tv_last_error.restype = ctypes.c_char_p
@@ -216,6 +218,17 @@ def chosen_path(a: AttnArgs) -> int:
 
 
 _ws_cache: dict = {}
+
+
+def verify_attn_noalloc(a: AttnArgs, stream=None):
+    """tv_verify_attn_noalloc on prepared arguments: the CUDA-core kernel with its split
+    scratch in the library's fixed device array (no workspace, no allocation)."""
+    rc = load().tv_verify_attn_noalloc(ctypes.byref(a), _stream(stream))
+    _check(rc, "tv_verify_attn_noalloc")
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load().tv_noalloc_scratch_bytes())
 
 
 def verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,

@@ -122,24 +122,29 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def kernel_traffic(kernel_tag: str):
+KERNEL_FILES = {"attn_tc": "k_attn_tc.cu", "attn_simt": "k_attn_simt.cu"}
+
+
+def kernel_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of the attention kernel from the committed ncu summary, when
-    it was taken on the current kernel source (hash match); else None."""
+    it was taken on the current source of that kernel's file (hash match); else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    ent = d.get(kernel_tag)
-    if not ent or ent.get("source_sha") != source_sha():
+    ent = d.get(f"{kernel}:{workload}")
+    if not ent or ent.get("source_sha") != source_sha(KERNEL_FILES[kernel]):
         return None
     return ent
 
 
-def source_sha():
+def source_sha(filename: str | None = None):
+    """sha256 prefix of one kernel source file (or of every csrc file)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_tree_04_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    names = [filename] if filename else sorted(os.listdir(csrc))
+    for fn in names:
         if fn.endswith((".cu", ".h")):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(f.read())
@@ -212,6 +217,9 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--quick", action="store_true",
+                    help="device-timed steps only (no end-to-end pass, no CPU baseline); "
+                         "used for profiler runs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -284,6 +292,15 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms, ams = float(t[0]), float(t[1])
 
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"quick": True, "workload": args.workload, "ms_per_step": ms,
+                              "attn_ms": ams, "attn_tflops": flops / (ams * 1e-3) / 1e12,
+                              "path": ["auto", "simt", "tcgen05"][path]}), flush=True)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+
     # ---- end to end through the public calls, host buffers in pinned memory ----------
     host = {k: _dev_float(inp, k, dev, pin=True) for k in
             ("q_latent", "q_pe", "kpe_tree", "c_kv", "k_pe")}
@@ -331,7 +348,7 @@ def main():
     attn_tflops = flops / (ams * 1e-3) / 1e12
     attn_gbs = byts / (ams * 1e-3) / 1e9
     kernel_tag = "attn_tc" if path == tv.PATH_TCGEN05 else "attn_simt"
-    trf = kernel_traffic(kernel_tag + ":" + args.workload)
+    trf = kernel_traffic(kernel_tag, args.workload)
     if path == tv.PATH_TCGEN05 or inp["kv_dtype"] == "bf16":
         roof = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
@@ -380,7 +397,7 @@ def main():
         "clocks": clk,
         "wall_s_timed": t_wall,
         "cpu_baseline": cpu,
-        "source_sha": source_sha(),
+        "source_sha": source_sha(KERNEL_FILES[kernel_tag]),
     }
     print(json.dumps(line), flush=True)
     if pg is not None:

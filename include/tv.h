@@ -76,6 +76,8 @@ typedef struct {
   int32_t page_size;         /* tokens per page (paged layout) */
   int32_t max_pages;         /* row stride of page_table, pages per sequence at most */
   int64_t kv_stride_b;       /* contiguous layout: cache rows per sequence */
+  int64_t num_rows;          /* rows in the c_kv / k_pe arrays; bounds the tensor-core
+                                path's TMA reads (0 = unknown: that path is not used) */
 } tv_cache_layout;
 
 /*

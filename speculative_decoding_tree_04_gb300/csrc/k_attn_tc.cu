@@ -1,0 +1,770 @@
+// k_attn_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) path of tv_verify_attn.
+//
+// Method: "The Precision Imperative: Validating Numerical Accuracy in a Custom CUDA
+// Attention Kernel" (§Context, §"Input Knowledge Required") and "The Golden Reference: A
+// Pivotal Moment in Building a Native DDTree Inference Engine" (§"The Absorb Form of
+// MLA"): for every (node, head) row, softmax over the visible keys of
+// scale*(q_latent.c_kv + q_pe.k_pe), then the softmax-weighted sum of c_kv rows.
+//
+// Shape of the work.  All H heads of all Q tree nodes of a sequence read the same latent
+// KV rows, so the rows (node, head) of one sequence form the M dimension of two dense
+// contractions: S = Q K^T (K = d_latent + d_rope = 576) and O = P V (N = d_latent = 512).
+// A 128-row tile's fp32 O accumulator alone (128 x 512 x 4 B = 256 KB) fills an SM's
+// tensor memory, leaving no room for S.  So each tile is served by a cluster of two CTAs
+// on two SMs that split the two contractions between them:
+//
+//   rank 0 ("S side"): holds the tile's queries in TMEM (A operand of QK^T), streams the
+//     keys' 64-key x 64-dim chunks through a TMA ring, computes S into one of two TMEM
+//     buffers, runs the masked online softmax (lazy rescaling: the running max only moves
+//     when it grows by more than 2^8), and ships each block's P (bf16, in the swizzled
+//     K-major layout the MMA reads), the per-row rescale factors and, at the end, the row
+//     sums to rank 1 with one bulk shared->shared copy per block.  It writes the lse.
+//   rank 1 ("O side"): streams the same keys' latent chunks as the V operand (MN-major
+//     B), accumulates O += P V in all 512 TMEM columns, applies the rare rescales, and at
+//     the end of the tile normalises O by the row sums and writes it out.
+//
+// Per 64-key block the S side does 2*128*64*576 flops and the O side 2*128*512*64, so
+// the pair is balanced to within 12%.  Warp roles per CTA (256 threads): warp 0 = TMA
+// producer, warp 1 = MMA issuer (and TMEM allocator), warp 2 = message bookkeeping on
+// rank 1, warps 4-7 = the row-parallel math (thread = tile row, matching TMEM lanes).
+// Tiles are handed out round-robin to the persistent clusters; long KV ranges may be
+// split across tiles and merged by the split combine kernel.
+//
+// Every wait is bounded (a wall-clock deadline); on expiry the kernel records
+// TV_ERR_TIMEOUT, tells the peer CTA, drains its tensor-core work, frees its TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "sm100_ptx.h"
+#include "tv_internal.h"
+
+namespace tv {
+namespace {
+
+using namespace ptx;
+
+constexpr int kDL = 512, kDR = 64, kBN = 64, kRows = 128;
+constexpr int kChunkBytes = kBN * 128;          // 64 keys x 64 bf16
+constexpr int kKChunks = 9;                     // 8 latent + 1 rope chunk per key block
+constexpr int kNK = 22;                         // S-side ring slots
+constexpr int kVStage = 4 * kChunkBytes;        // 256 latent dims x 64 keys
+constexpr int kNV = 5;                          // O-side ring stages
+constexpr int kMsgAlpha = 16384, kMsgL = 16896, kMsgHdr = 17408, kMsgBytes = 17424;
+constexpr int kMsgStride = 18432;
+constexpr int kThreads = 256;
+constexpr int kSideA = kNK * kChunkBytes + 2 * kMsgStride;   // S side: ring + staging
+constexpr int kSideB = kNV * kVStage + 2 * kMsgStride;       // O side: ring + inbox
+constexpr int kSmemBytes = (kSideA > kSideB ? kSideA : kSideB) + 1024;
+constexpr uint32_t kTmQ = 0, kTmS0 = 288, kTmS1 = 352;       // S-side TMEM columns
+constexpr uint32_t kFlagFirst = 1, kFlagRescale = 2, kFlagFinal = 4;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
+
+struct TcParams {
+  const __nv_bfloat16* q_latent;
+  const __nv_bfloat16* q_pe;
+  const int32_t* page_table;
+  int64_t kv_stride_b;
+  const int32_t* prefix_len;
+  const uint64_t* anc;
+  float* out;
+  float* lse;
+  float* ws_out;
+  float* ws_lse;
+  int32_t* status;
+  int64_t rows_total;  // B*Q*H
+  int32_t max_pages;
+  int32_t B, H, Q, max_prefix;
+  int32_t tiles_per_seq, splits, chunk, n_items;
+  int32_t paged;
+  float scale_log2;
+};
+
+struct Shared {
+  uint64_t k_full[kNK], k_empty[kNK];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t q_ready, q_free, pdst_free[2];
+  uint64_t v_full[kNV], v_empty[kNV];
+  uint64_t p_full[2], p_consumed[2];
+  uint64_t drain, job_full, corr_done, epi_done, final_bar;
+  uint32_t tmem_base;
+  volatile int abort;
+  volatile int job_type, job_buf;
+};
+
+struct Item {
+  int b, t, s, P, nb;
+  int64_t k0;
+  bool bad;
+};
+
+__device__ __forceinline__ Item decode(const TcParams& p, int item) {
+  Item it;
+  it.t = item % p.tiles_per_seq;
+  const int bs = item / p.tiles_per_seq;
+  it.s = bs % p.splits;
+  it.b = bs / p.splits;
+  it.P = p.prefix_len[it.b];
+  const int64_t kv_len = (int64_t)it.P + p.Q;
+  it.bad = it.P < 0 || it.P > p.max_prefix ||
+           (p.paged ? kv_len > (int64_t)p.max_pages * kBN : kv_len > p.kv_stride_b);
+  it.k0 = (int64_t)it.s * p.chunk;
+  int64_t k1 = it.k0 + p.chunk < kv_len ? it.k0 + p.chunk : kv_len;
+  if (it.bad) k1 = it.k0;
+  it.nb = k1 > it.k0 ? (int)((k1 - it.k0 + kBN - 1) / kBN) : 0;
+  return it;
+}
+
+__device__ __forceinline__ void raise_abort(Shared& sh, int32_t* status, int code) {
+  if (!sh.abort) {
+    sh.abort = 1;
+    report(status, code);
+    // tell the peer CTA so that its waits end quickly too
+    const uint32_t peer = map_to_rank(smem_u32((const void*)&sh.abort), cluster_rank() ^ 1u);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1) : "memory");
+  }
+}
+
+// Bounded wait on phase `parity` of a local mbarrier.
+__device__ __forceinline__ bool wait_bar(Shared& sh, uint64_t* bar, uint32_t parity,
+                                         int32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (sh.abort) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      raise_abort(sh, status, TV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ int64_t block_row0(const TcParams& p, const Item& it, int j) {
+  const int64_t key0 = it.k0 + (int64_t)j * kBN;
+  if (p.paged) return (int64_t)p.page_table[(int64_t)it.b * p.max_pages + key0 / kBN] * kBN;
+  return (int64_t)it.b * p.kv_stride_b + key0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ===================================================================================
+// rank 0: QK^T + softmax
+// ===================================================================================
+__device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUtensorMap* map_kpe,
+                       Shared& sh, unsigned char* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* ring = smem;
+  unsigned char* stage = smem + kNK * kChunkBytes;
+  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: 9 chunks per key block -------------------------
+    if (lane == 0) {
+      prefetch_tensormap(map_ckv);
+      prefetch_tensormap(map_kpe);
+      uint32_t kc = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        for (int j = 0; j < it.nb; ++j) {
+          const int row0 = (int)block_row0(p, it, j);
+          for (int c = 0; c < kKChunks; ++c, ++kc) {
+            const uint32_t slot = kc % kNK;
+            if (!wait_bar(sh, &sh.k_empty[slot], ((kc / kNK) & 1) ^ 1, p.status)) return;
+            mbar_arrive_expect_tx(&sh.k_full[slot], kChunkBytes);
+            if (c < 8)
+              tma_load_2d(ring + slot * kChunkBytes, map_ckv, 64 * c, row0, &sh.k_full[slot]);
+            else
+              tma_load_2d(ring + slot * kChunkBytes, map_kpe, 0, row0, &sh.k_full[slot]);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: S = Q K^T -----------------------------------------
+    if (lane == 0) {
+      uint32_t kc = 0, sc = 0, qc = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        if (it.nb == 0) continue;
+        if (!wait_bar(sh, &sh.q_ready, qc & 1, p.status)) break;
+        ++qc;
+        tc_fence_after();
+        for (int j = 0; j < it.nb && !sh.abort; ++j, ++sc) {
+          const uint32_t sb = sc & 1;
+          if (!wait_bar(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
+          tc_fence_after();
+          const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
+          for (int c = 0; c < kKChunks; ++c, ++kc) {
+            const uint32_t slot = kc % kNK;
+            if (!wait_bar(sh, &sh.k_full[slot], (kc / kNK) & 1, p.status)) break;
+            tc_fence_after();
+            const uint32_t sa = smem_u32(ring + slot * kChunkBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(d, tmem + kTmQ + 32 * c + 8 * kk, smem_desc(sa + 32 * kk, 16, 1024, 2),
+                     kIdescQK, (c | kk) != 0);
+            mma_commit(&sh.k_empty[slot]);
+          }
+          mma_commit(&sh.s_full[sb]);
+        }
+        mma_commit(&sh.q_free);
+      }
+      mma_commit(&sh.final_bar);
+      wait_bar(sh, &sh.final_bar, 0, p.status);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroup: thread r owns tile row r ------------------
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t peer = cluster_rank() ^ 1u;
+    unsigned char* peer_inbox_local = smem + kNV * kVStage;  // same offset in the peer
+    uint32_t sc = 0, qc = 0, mc = 0;
+    for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+      const Item it = decode(p, item);
+      const int trow = it.t * kRows + r;
+      const bool vrow = trow < p.Q * p.H;
+      const int64_t grow = (int64_t)it.b * p.Q * p.H + trow;
+      float* lse_dst = p.splits == 1 ? p.lse + grow : p.ws_lse + (int64_t)it.s * p.rows_total + grow;
+      if (it.bad && r == 0 && it.t == 0 && it.s == 0) report(p.status, TV_ERR_BOUNDS);
+      if (it.nb == 0) {
+        if (vrow) *lse_dst = -INFINITY;
+        continue;
+      }
+      const uint64_t anc = vrow ? p.anc[(int64_t)it.b * p.Q + trow / p.H] : 0ull;
+      const int64_t kv_end = (int64_t)it.P + p.Q;
+      const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
+
+      // ---- queries of this row into TMEM columns [0, 288) ----
+      // (every wait of the warpgroup ends in a barrier that agrees on its outcome, so that
+      // no thread is left waiting in a barrier for one that gave up)
+      if (!named_sync_and(1, 128, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) break;
+      ++qc;
+      tc_fence_after();
+      {
+        const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + grow * kDL);
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q_pe + grow * kDR);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kKChunks; c0 += 3) {
+          uint32_t w[3][32];
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) {
+            const int c = c0 + cc;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (vrow) v = c < 8 ? __ldg(ql + 8 * c + e) : __ldg(qr + e);
+              w[cc][4 * e + 0] = v.x;
+              w[cc][4 * e + 1] = v.y;
+              w[cc][4 * e + 2] = v.z;
+              w[cc][4 * e + 3] = v.w;
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) tmem_st32(tmem + lane_base + kTmQ + 32 * (c0 + cc), w[cc]);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sh.q_ready);
+
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.nb; ++j, ++sc, ++mc) {
+        const uint32_t sb = sc & 1;
+        if (!named_sync_and(1, 128, wait_bar(sh, &sh.s_full[sb], (sc >> 1) & 1, p.status))) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0), sr);
+        tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0) + 32, sr + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&sh.s_empty[sb]);
+
+        float x[64];
+        const int64_t key0 = it.k0 + (int64_t)j * kBN;
+        const bool need_mask = key0 + kBN > it.P || key0 + kBN > k1;
+        float bm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          float v = __uint_as_float(sr[k]) * p.scale_log2;
+          if (need_mask) {
+            const int64_t key = key0 + k;
+            const bool vis = key < k1 && (key < it.P || ((anc >> (int)(key - it.P)) & 1ull));
+            v = vis ? v : -INFINITY;
+          }
+          x[k] = v;
+          bm = fmaxf(bm, v);
+        }
+        float alpha = 1.f;
+        bool resc = false;
+        if (bm > m + kRescaleThreshold) {
+          alpha = exp2f(m - bm);
+          resc = l > 0.f;
+          m = bm;
+        }
+        float sum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const float p0 = x[k] == -INFINITY ? 0.f : exp2f(x[k] - m);
+          const float p1 = x[k + 1] == -INFINITY ? 0.f : exp2f(x[k + 1] - m);
+          sum += p0 + p1;
+          pk[k >> 1] = pack_bf16(p0, p1);
+        }
+        l = l * alpha + sum;
+
+        // ---- ship P, alpha (and the row sums on the last block) to rank 1 ----
+        const uint32_t pb = mc & 1;
+        unsigned char* msg = stage + pb * kMsgStride;
+        if (r == 0) bulk_wait_read<1>();
+        named_sync(1, 128);
+        {
+          unsigned char* rowp = msg + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          reinterpret_cast<float*>(msg + kMsgAlpha)[r] = alpha;
+          if (j == it.nb - 1) reinterpret_cast<float*>(msg + kMsgL)[r] = l;
+        }
+        fence_proxy_async_smem();
+        const bool any_resc = named_sync_or(1, 128, resc);
+        if (r == 0) {
+          uint32_t flags = (j == 0 ? kFlagFirst : 0u) | (j == it.nb - 1 ? kFlagFinal : 0u) |
+                           ((any_resc && j > 0) ? kFlagRescale : 0u);
+          *reinterpret_cast<volatile uint32_t*>(msg + kMsgHdr) = flags;
+          fence_proxy_async_smem();
+          if (wait_bar(sh, &sh.pdst_free[pb], ((mc >> 1) & 1) ^ 1, p.status)) {
+            const uint32_t dst = map_to_rank(smem_u32(peer_inbox_local + pb * kMsgStride), peer);
+            const uint32_t bar = map_to_rank(smem_u32(&sh.p_full[pb]), peer);
+            bulk_copy_to_cluster(dst, msg, kMsgBytes, bar);
+            bulk_commit();
+          }
+        }
+        __syncwarp();
+      }
+      if (vrow && !sh.abort)
+        *lse_dst = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+}
+
+// ===================================================================================
+// rank 1: O += P V, rescale, epilogue
+// ===================================================================================
+__device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh,
+                       unsigned char* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* vring = smem;
+  unsigned char* inbox = smem + kNV * kVStage;
+  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: latent chunks as V -----------------------------
+    if (lane == 0) {
+      prefetch_tensormap(map_ckv);
+      uint32_t vc = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        for (int j = 0; j < it.nb; ++j) {
+          const int row0 = (int)block_row0(p, it, j);
+          for (int h = 0; h < 2; ++h, ++vc) {
+            const uint32_t st = vc % kNV;
+            if (!wait_bar(sh, &sh.v_empty[st], ((vc / kNV) & 1) ^ 1, p.status)) return;
+            mbar_arrive_expect_tx(&sh.v_full[st], kVStage);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              tma_load_2d(vring + st * kVStage + q * kChunkBytes, map_ckv, 256 * h + 64 * q,
+                          row0, &sh.v_full[st]);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: O += P V ------------------------------------------
+    if (lane == 0) {
+      uint32_t vc = 0, mc = 0, ic = 0, dc = 0, cc = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        if (it.nb == 0) continue;
+        if (ic > 0 && !wait_bar(sh, &sh.epi_done, (ic - 1) & 1, p.status)) break;
+        tc_fence_after();
+        uint32_t last_pb = 0;
+        bool ok = true;
+        for (int j = 0; j < it.nb && ok; ++j, ++mc) {
+          const uint32_t pb = mc & 1;
+          last_pb = pb;
+          if (!wait_bar(sh, &sh.p_full[pb], (mc >> 1) & 1, p.status)) { ok = false; break; }
+          const uint32_t flags =
+              *reinterpret_cast<volatile uint32_t*>(inbox + pb * kMsgStride + kMsgHdr);
+          if (flags & kFlagRescale) {
+            mma_commit(&sh.drain);
+            if (!wait_bar(sh, &sh.drain, dc & 1, p.status)) { ok = false; break; }
+            ++dc;
+            sh.job_type = 1;
+            sh.job_buf = (int)pb;
+            mbar_arrive(&sh.job_full);
+            if (!wait_bar(sh, &sh.corr_done, cc & 1, p.status)) { ok = false; break; }
+            ++cc;
+            tc_fence_after();
+          }
+          const uint32_t pa = smem_u32(inbox + pb * kMsgStride);
+          for (int h = 0; h < 2; ++h, ++vc) {
+            const uint32_t st = vc % kNV;
+            if (!wait_bar(sh, &sh.v_full[st], (vc / kNV) & 1, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t va = smem_u32(vring + st * kVStage);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + 256 * h, smem_desc(pa + 32 * kk, 16, 1024, 2),
+                     smem_desc(va + 2048 * kk, 8192, 1024, 2), kIdescPV, (j | kk) != 0);
+            mma_commit(&sh.v_empty[st]);
+          }
+          mma_commit(&sh.p_consumed[pb]);
+        }
+        if (!ok) break;
+        mma_commit(&sh.drain);
+        if (!wait_bar(sh, &sh.drain, dc & 1, p.status)) break;
+        ++dc;
+        sh.job_type = 2;
+        sh.job_buf = (int)last_pb;
+        mbar_arrive(&sh.job_full);
+        ++ic;
+      }
+      if (!sh.abort && ic > 0) wait_bar(sh, &sh.epi_done, (ic - 1) & 1, p.status);
+      sh.job_type = 0;  // exit
+      mbar_arrive(&sh.job_full);
+      mma_commit(&sh.final_bar);
+      wait_bar(sh, &sh.final_bar, 0, p.status);
+    }
+  } else if (warp == 2) {
+    // ---------------- inbox bookkeeping: re-arm and hand buffers back ---------------
+    if (lane == 0) {
+      const uint32_t peer = cluster_rank() ^ 1u;
+      uint32_t mc = 0, ic = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        if (it.nb == 0) continue;
+        for (int j = 0; j < it.nb; ++j, ++mc) {
+          const uint32_t pb = mc & 1;
+          if (!wait_bar(sh, &sh.p_consumed[pb], (mc >> 1) & 1, p.status)) return;
+          if (j == it.nb - 1 && !wait_bar(sh, &sh.epi_done, ic & 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.p_full[pb], kMsgBytes);
+          mbar_arrive_remote(map_to_rank(smem_u32(&sh.pdst_free[pb]), peer));
+        }
+        ++ic;
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- rescale / epilogue warpgroup: thread r owns tile row r -------
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    uint32_t jc = 0;
+    for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+      const Item it = decode(p, item);
+      const int trow = it.t * kRows + r;
+      const bool vrow = trow < p.Q * p.H;
+      const int64_t grow = (int64_t)it.b * p.Q * p.H + trow;
+      float* dst = p.splits == 1 ? p.out + grow * kDL
+                                 : p.ws_out + ((int64_t)it.s * p.rows_total + grow) * kDL;
+      if (it.nb == 0) {
+        if (vrow)
+          for (int c = 0; c < kDL / 4; ++c)
+            reinterpret_cast<float4*>(dst)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
+      for (;;) {
+        // the four warps work on disjoint TMEM lanes; each warp agrees on the outcome
+        if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.job_full, jc & 1, p.status))) return;
+        ++jc;
+        const int type = sh.job_type, pb = sh.job_buf;
+        tc_fence_after();
+        if (type == 1) {
+          const float alpha = reinterpret_cast<const float*>(inbox + pb * kMsgStride + kMsgAlpha)[r];
+          // warp-uniform decision: the TMEM loads and stores below are warp-collective
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < 16; ++c) {
+              uint32_t v[32];
+              __syncwarp();
+              tmem_ld32(tmem + lane_base + 32 * c, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tmem_st32(tmem + lane_base + 32 * c, v);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(&sh.corr_done);
+        } else if (type == 2) {
+          const float lr = reinterpret_cast<const float*>(inbox + pb * kMsgStride + kMsgL)[r];
+          const float inv = lr > 0.f ? 1.f / lr : 0.f;
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            uint32_t v[32];
+            __syncwarp();
+            tmem_ld32(tmem + lane_base + 32 * c, v);
+            tmem_wait_ld();
+            if (vrow) {
+              float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                d4[e] = make_float4(__uint_as_float(v[4 * e]) * inv, __uint_as_float(v[4 * e + 1]) * inv,
+                                    __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&sh.epi_done);
+          break;
+        } else {
+          return;  // exit job (only after an abort)
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
+               const __grid_constant__ CUtensorMap map_kpe) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ Shared sh;
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t rank = cluster_rank();
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNK; ++i) {
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_empty[i], 1);
+    }
+    for (int i = 0; i < kNV; ++i) {
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.s_empty[i], 128);
+      mbar_init(&sh.pdst_free[i], 1);
+      mbar_init(&sh.p_full[i], 1);
+      mbar_init(&sh.p_consumed[i], 1);
+    }
+    mbar_init(&sh.q_ready, 128);
+    mbar_init(&sh.q_free, 1);
+    mbar_init(&sh.drain, 1);
+    mbar_init(&sh.job_full, 1);
+    mbar_init(&sh.corr_done, 128);
+    mbar_init(&sh.epi_done, 128);
+    mbar_init(&sh.final_bar, 1);
+    sh.abort = 0;
+    sh.job_type = 0;
+    sh.job_buf = 0;
+    if (rank == 1) {
+      // both inbox buffers start armed for the first two messages
+      mbar_arrive_expect_tx(&sh.p_full[0], kMsgBytes);
+      mbar_arrive_expect_tx(&sh.p_full[1], kMsgBytes);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // barriers of both CTAs exist before any remote arrive or copy
+
+  if (rank == 0)
+    s_side(p, &map_ckv, &map_kpe, sh, smem);
+  else
+    o_side(p, &map_ckv, sh, smem);
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(sh.tmem_base, 512);
+  cluster_sync();  // neither CTA leaves while the other may still touch its memory
+}
+
+// ---- host side -----------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+int g_max_clusters[64] = {};
+std::mutex g_mu;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t row_bytes) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int max_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_max_clusters[dev] == 0) {
+    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      int sms = current_sm_count();
+      n = sms / 2;
+    }
+    g_max_clusters[dev] = n;
+  }
+  return g_max_clusters[dev];
+}
+
+}  // namespace
+
+bool tc_supported(const tv_attn_args* a) {
+  return a->q_dt == TV_BF16 && a->kv_dt == TV_BF16 && a->d_latent == kDL && a->d_rope == kDR &&
+         a->cache.num_rows > 0 && a->cache.num_rows < (1ll << 31) &&
+         (a->cache.page_table == nullptr || a->cache.page_size == kBN);
+}
+
+TcPlan tc_plan(const tv_attn_args* a) {
+  TcPlan p{};
+  const int clusters = max_clusters() > 0 ? max_clusters() : 74;
+  p.clusters = clusters;
+  p.tiles_per_seq = (a->Q * a->H + kRows - 1) / kRows;
+  const int64_t tiles = (int64_t)a->B * p.tiles_per_seq;
+  const int64_t kv_max = (int64_t)a->max_prefix_len + a->Q;
+  int splits = a->num_splits;
+  if (splits <= 0) {
+    splits = 1;
+    if (tiles < 2LL * clusters) {
+      const int64_t want = (2LL * clusters + tiles - 1) / std::max<int64_t>(tiles, 1);
+      const int64_t cap = std::max<int64_t>(1, kv_max / 512);
+      splits = (int)std::max<int64_t>(1, std::min(want, cap));
+    }
+  }
+  int64_t chunk = (kv_max + splits - 1) / splits;
+  chunk = (chunk + kBN - 1) / kBN * kBN;
+  if (chunk < kBN) chunk = kBN;
+  p.chunk = (int)chunk;
+  p.splits = (int)((kv_max + chunk - 1) / chunk);
+  if (p.splits < 1) p.splits = 1;
+  p.n_items = (int)(tiles * p.splits);
+  return p;
+}
+
+size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) {
+  if (p.splits <= 1) return 0;
+  const size_t rows = (size_t)a->B * a->Q * a->H;
+  const size_t out_b = ((size_t)p.splits * rows * a->d_latent * 4 + 255) / 256 * 256;
+  const size_t lse_b = ((size_t)p.splits * rows * 4 + 255) / 256 * 256;
+  return out_b + lse_b;
+}
+
+cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cudaStream_t st) {
+  if (!get_encode()) return cudaErrorNotSupported;
+  if (max_clusters() <= 0) return cudaErrorNotSupported;
+  CUtensorMap mc, mk;
+  if (!make_map(&mc, a->c_kv, kDL, (uint64_t)a->cache.num_rows, (uint64_t)a->ckv_row_stride * 2))
+    return cudaErrorInvalidValue;
+  if (!make_map(&mk, a->k_pe, kDR, (uint64_t)a->cache.num_rows, (uint64_t)a->kpe_row_stride * 2))
+    return cudaErrorInvalidValue;
+  TcParams p{};
+  p.q_latent = (const __nv_bfloat16*)a->q_latent;
+  p.q_pe = (const __nv_bfloat16*)a->q_pe;
+  p.page_table = a->cache.page_table;
+  p.kv_stride_b = a->cache.kv_stride_b;
+  p.prefix_len = a->prefix_len;
+  p.anc = a->anc;
+  p.out = a->out;
+  p.lse = a->lse;
+  const size_t rows = (size_t)a->B * a->Q * a->H;
+  p.ws_out = (float*)ws;
+  p.ws_lse = ws ? (float*)((char*)ws + ((size_t)pl.splits * rows * a->d_latent * 4 + 255) / 256 * 256)
+                : nullptr;
+  p.status = a->status;
+  p.rows_total = (int64_t)rows;
+  p.max_pages = a->cache.max_pages;
+  p.B = a->B;
+  p.H = a->H;
+  p.Q = a->Q;
+  p.max_prefix = a->max_prefix_len;
+  p.tiles_per_seq = pl.tiles_per_seq;
+  p.splits = pl.splits;
+  p.chunk = pl.chunk;
+  p.n_items = pl.n_items;
+  p.paged = a->cache.page_table != nullptr;
+  p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+  if (p.n_items == 0) return cudaSuccess;
+
+  const int ncl = std::min(pl.clusters, pl.n_items);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ncl);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, mc, mk);
+  if (e != cudaSuccess || pl.splits == 1) return e;
+  return launch_combine(p.ws_out, p.ws_lse, pl.splits, (int64_t)rows, a->d_latent, a->out,
+                        a->lse, st);
+}
+
+}  // namespace tv

@@ -74,9 +74,20 @@ int check_attn(const tv_attn_args* a) {
   return TV_OK;
 }
 
+// Tensor cores when the shape is the absorbed-MLA one they implement (bf16, d_latent 512,
+// d_rope 64, known cache size) and the problem has at least two full 128-row tiles;
+// CUDA cores otherwise.
 int resolve_path(const tv_attn_args* a) {
-  if (a->path == TV_PATH_TCGEN05)
-    return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: tensor-core path not available for these arguments%s");
+  const bool tc_ok = tv::tc_supported(a);
+  if (a->path == TV_PATH_TCGEN05) {
+    if (!tc_ok)
+      return fail(TV_ERR_UNSUPPORTED,
+                  "tv_verify_attn: tensor-core path needs bf16 q and cache, d_latent 512, "
+                  "d_rope 64, 64-token pages and cache.num_rows%s");
+    return TV_PATH_TCGEN05;
+  }
+  if (a->path == TV_PATH_AUTO && tc_ok && (int64_t)a->B * a->Q * a->H >= 256)
+    return TV_PATH_TCGEN05;
   if (!tv::simt_supported(a))
     return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: shape not supported%s");
   return TV_PATH_SIMT;
@@ -166,6 +177,7 @@ size_t tv_verify_attn_workspace_size(const tv_attn_args* a) {
   if (check_attn(a) != TV_OK) return 0;
   const int path = resolve_path(a);
   if (path == TV_PATH_SIMT) return tv::simt_workspace(a, tv::simt_plan(a, sm_count()));
+  if (path == TV_PATH_TCGEN05) return tv::tc_workspace(a, tv::tc_plan(a));
   return 0;
 }
 
@@ -178,6 +190,14 @@ int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void
   if (path < 0) return path;
   if (workspace && ((uintptr_t)workspace & 255u))
     return fail(TV_ERR_WORKSPACE, "tv_verify_attn: workspace must be 256-byte aligned%s");
+  if (path == TV_PATH_TCGEN05) {
+    const tv::TcPlan plan = tv::tc_plan(a);
+    const size_t need = tv::tc_workspace(a, plan);
+    if (need > 0 && (!workspace || ws_bytes < need))
+      return fail(TV_ERR_WORKSPACE, "tv_verify_attn: workspace smaller than tv_verify_attn_workspace_size()%s");
+    cudaError_t e = tv::launch_attn_tc(a, plan, workspace, (cudaStream_t)stream);
+    return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_verify_attn (tensor cores)");
+  }
   const tv::SimtPlan plan = tv::simt_plan(a, sm_count());
   const size_t need = tv::simt_workspace(a, plan);
   if (need > 0 && (!workspace || ws_bytes < need))

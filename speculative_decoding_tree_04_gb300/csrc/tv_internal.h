@@ -53,6 +53,19 @@ bool simt_supported(const tv_attn_args* a);
 cudaError_t launch_attn_simt(const tv_attn_args* a, const SimtPlan& p, void* ws,
                              cudaStream_t st);
 
+// Work decomposition of the tensor-core path.
+struct TcPlan {
+  int clusters;       // persistent 2-CTA clusters launched (at most)
+  int tiles_per_seq;  // ceil(Q*H / 128)
+  int splits;         // KV splits
+  int chunk;          // keys per split (multiple of 64)
+  int n_items;        // B * tiles_per_seq * splits
+};
+bool tc_supported(const tv_attn_args* a);
+TcPlan tc_plan(const tv_attn_args* a);
+size_t tc_workspace(const tv_attn_args* a, const TcPlan& p);
+cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& p, void* ws, cudaStream_t st);
+
 // Split-KV combine: partial (out_s, lse_s) for s < splits -> final out, lse.
 cudaError_t launch_combine(const float* ws_out, const float* ws_lse, int splits,
                            int64_t rows, int DL, float* out, float* lse, cudaStream_t st);

@@ -35,7 +35,8 @@ class TVError(RuntimeError):
 
 class CacheLayout(ctypes.Structure):
     _fields_ = [("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
-                ("max_pages", ctypes.c_int32), ("kv_stride_b", ctypes.c_int64)]
+                ("max_pages", ctypes.c_int32), ("kv_stride_b", ctypes.c_int64),
+                ("num_rows", ctypes.c_int64)]
 
 
 class AttnArgs(ctypes.Structure):
@@ -138,12 +139,13 @@ def build_visibility(parent, anc, depth, dense_mask=None, status=None, stream=No
     _check(rc, "tv_build_visibility")
 
 
-def make_cache(page_table=None, page_size=64, kv_stride_b=0) -> CacheLayout:
+def make_cache(page_table=None, page_size=64, kv_stride_b=0, num_rows=0) -> CacheLayout:
+    """Cache geometry; num_rows = rows of the c_kv / k_pe arrays (0 = unknown)."""
     if page_table is not None:
         _need_cuda(page_table)
         assert page_table.dtype == torch.int32 and page_table.is_contiguous()
-        return CacheLayout(page_table.data_ptr(), page_size, page_table.shape[1], 0)
-    return CacheLayout(None, page_size, 0, kv_stride_b)
+        return CacheLayout(page_table.data_ptr(), page_size, page_table.shape[1], 0, num_rows)
+    return CacheLayout(None, page_size, 0, kv_stride_b, num_rows)
 
 
 def rope_neox(x, out, prefix_len, depth, base=10000.0, cache: CacheLayout | None = None,
@@ -196,7 +198,8 @@ def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_
     a.q_latent, a.q_pe = q_latent.data_ptr(), q_pe.data_ptr()
     a.c_kv, a.k_pe = c_kv.data_ptr(), k_pe.data_ptr()
     a.ckv_row_stride, a.kpe_row_stride = c_kv.stride(0), k_pe.stride(0)
-    a.cache = make_cache(page_table, page_size, kv_stride_b)
+    a.cache = make_cache(page_table, page_size, kv_stride_b,
+                         min(c_kv.shape[0], k_pe.shape[0]))
     a.prefix_len = prefix_len.data_ptr()
     a.max_prefix_len = int(max_prefix_len)
     a.anc = anc.data_ptr()

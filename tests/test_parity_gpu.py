@@ -57,16 +57,38 @@ def test_workload_parity_simt(name, splits):
     print(name, "splits", splits, "out", e_out, "lse", e_lse)
 
 
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_workload_parity_tc_cfg3(splits):
+    inp = synth.generate("cfg3_bf16")
+    step, g, o = run_pair(inp, path=tv.PATH_TCGEN05, num_splits=splits)
+    print("cfg3 tc splits", splits, check_step(inp, g, o))
+
+
+@pytest.mark.parametrize("path", [tv.PATH_SIMT, tv.PATH_TCGEN05])
+def test_workload_parity_cfg4_both_paths(path):
+    inp = synth.generate("cfg4_bf16")
+    step, g, o = run_pair(inp, path=path)
+    print("cfg4 path", path, check_step(inp, g, o))
+
+
+def test_auto_path_is_tensor_cores_for_large_bf16():
+    for name in ("cfg4_bf16", "cfg5_bf16"):
+        inp = synth.generate(name, B=2)
+        assert VerifyStep(inp).chosen_path() == tv.PATH_TCGEN05
+    assert VerifyStep(synth.generate("cfg2_fp32")).chosen_path() == tv.PATH_SIMT
+
+
 def test_workload_parity_cfg4_auto():
     inp = synth.generate("cfg4_bf16")
     step, g, o = run_pair(inp)
     print("cfg4 path", step.chosen_path(), check_step(inp, g, o))
 
 
-def test_workload_parity_cfg5_sampled():
+@pytest.mark.parametrize("path", [tv.PATH_AUTO, tv.PATH_SIMT])
+def test_workload_parity_cfg5_sampled(path):
     inp = synth.generate("cfg5_bf16")
     seqs = synth.sample_sequences(inp, 4)
-    step, g, o = run_pair(inp, seqs=seqs)
+    step, g, o = run_pair(inp, path=path, seqs=seqs)
     print("cfg5 path", step.chosen_path(), "seqs", seqs, check_step(inp, g, o, seqs=seqs))
 
 
@@ -88,6 +110,34 @@ EDGE = [
 def test_edge_cases(desc, kw, dtype):
     inp = synth.generate(seed=zlib.crc32(desc.encode()) % 1000, dtype=dtype, **kw)
     step, g, o = run_pair(inp)
+    check_step(inp, g, o)
+
+
+EDGE_TC = [
+    ("tc q_len 1", dict(B=3, H=8, Q=1, prefix=(5, 300))),
+    ("tc prefix 0", dict(B=2, H=8, Q=9, prefix=(0, 0))),
+    ("tc mid-page prefix, paged", dict(B=3, H=16, Q=17, prefix=(100, 130), paged=True)),
+    ("tc 33 heads", dict(B=2, H=33, Q=5, prefix=(60, 700), paged=True)),
+    ("tc q_len 64 wide", dict(B=2, H=4, Q=64, prefix=(1, 200), tree="wide")),
+    ("tc chain, contiguous", dict(B=2, H=64, Q=12, prefix=(64, 128), tree="chain")),
+    ("tc sharp softmax (frequent rescales)", dict(B=2, H=16, Q=9, prefix=(300, 900), q_var=0.02,
+                                                  paged=True)),
+]
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+@pytest.mark.parametrize("desc,kw", EDGE_TC, ids=[e[0] for e in EDGE_TC])
+def test_edge_cases_tensor_cores(desc, kw, splits):
+    inp = synth.generate(seed=zlib.crc32(desc.encode()) % 1000, dtype="bf16", DL=512, DR=64,
+                         **kw)
+    step, g, o = run_pair(inp, path=tv.PATH_TCGEN05, num_splits=splits)
+    check_step(inp, g, o)
+
+
+def test_sharp_softmax_simt():
+    inp = synth.generate(seed=5, dtype="fp32", B=2, H=16, Q=9, DL=512, DR=64,
+                         prefix=(300, 900), q_var=0.02)
+    step, g, o = run_pair(inp, path=tv.PATH_SIMT)
     check_step(inp, g, o)
 
 

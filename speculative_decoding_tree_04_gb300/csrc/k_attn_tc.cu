@@ -13,8 +13,9 @@
 // tensor memory, leaving no room for S.  So each tile is served by a cluster of two CTAs
 // on two SMs that split the two contractions between them:
 //
-//   rank 0 ("S side"): holds the tile's queries in TMEM (A operand of QK^T), streams the
-//     keys' 64-key x 64-dim chunks through a TMA ring, computes S into one of two TMEM
+//   rank 0 ("S side"): holds the tile's queries in TMEM (A operand of QK^T), streams each
+//     64-key block through a two-stage TMA ring (two 3-D boxes of 4 latent chunks each plus
+//     the rope chunk: few, large requests keep the TMA engine busy), computes S into one of two TMEM
 //     buffers, runs the masked online softmax (lazy rescaling: the running max only moves
 //     when it grows by more than 2^8), and ships each block's P (bf16, in the swizzled
 //     K-major layout the MMA reads), the per-row rescale factors and, at the end, the row
@@ -25,8 +26,10 @@
 //
 // Per 64-key block the S side does 2*128*64*576 flops and the O side 2*128*512*64, so
 // the pair is balanced to within 12%.  Warp roles per CTA (256 threads): warp 0 = TMA
-// producer, warp 1 = MMA issuer (and TMEM allocator), warp 2 = message bookkeeping on
-// rank 1, warps 4-7 = the row-parallel math (thread = tile row, matching TMEM lanes).
+// producer, warp 1 = MMA issuer (and TMEM allocator), warp 2 = message sender on rank 0
+// and message bookkeeping on rank 1, warps 4-7 = the row-parallel math (thread = tile
+// row, matching TMEM lanes).  Messages travel through 2 staging buffers on rank 0 and 4
+// inbox buffers on rank 1, so the softmax never waits for the peer's round trip.
 // Tiles are handed out round-robin to the persistent clusters; long KV ranges may be
 // split across tiles and merged by the split combine kernel.
 //
@@ -52,14 +55,20 @@ using namespace ptx;
 constexpr int kDL = 512, kDR = 64, kBN = 64, kRows = 128;
 constexpr int kChunkBytes = kBN * 128;          // 64 keys x 64 bf16
 constexpr int kKChunks = 9;                     // 8 latent + 1 rope chunk per key block
-constexpr int kNK = 22;                         // S-side ring slots
-constexpr int kVStage = 4 * kChunkBytes;        // 256 latent dims x 64 keys
-constexpr int kNV = 5;                          // O-side ring stages
+constexpr int kHalf = 4 * kChunkBytes;          // 4 latent chunks: one 3-D TMA box
+constexpr int kNL = 4;                          // latent ring stages (half key blocks)
+constexpr int kNR = 2;                          // S-side rope ring stages
 constexpr int kMsgAlpha = 16384, kMsgL = 16896, kMsgHdr = 17408, kMsgBytes = 17424;
 constexpr int kMsgStride = 18432;
+constexpr int kNStage = 2;                      // S-side staging buffers
+constexpr int kNInbox = 4;                      // O-side inbox buffers
 constexpr int kThreads = 256;
-constexpr int kSideA = kNK * kChunkBytes + 2 * kMsgStride;   // S side: ring + staging
-constexpr int kSideB = kNV * kVStage + 2 * kMsgStride;       // O side: ring + inbox
+// Shared memory, from offset 0 in both CTAs: the latent ring (multicast by rank 1 into
+// both CTAs at the same offset), then on rank 0 the rope ring and the staging buffers,
+// on rank 1 the inbox.
+constexpr int kLatBytes = kNL * kHalf;
+constexpr int kSideA = kLatBytes + kNR * kChunkBytes + kNStage * kMsgStride;
+constexpr int kSideB = kLatBytes + kNInbox * kMsgStride;
 constexpr int kSmemBytes = (kSideA > kSideB ? kSideA : kSideB) + 1024;
 constexpr uint32_t kTmQ = 0, kTmS0 = 288, kTmS1 = 352;       // S-side TMEM columns
 constexpr uint32_t kFlagFirst = 1, kFlagRescale = 2, kFlagFinal = 4;
@@ -90,11 +99,11 @@ struct TcParams {
 };
 
 struct Shared {
-  uint64_t k_full[kNK], k_empty[kNK];
+  uint64_t lat_full[kNL], lat_consumed[kNL], lat_empty[kNL];
+  uint64_t rope_full[kNR], rope_empty[kNR];
   uint64_t s_full[2], s_empty[2];
-  uint64_t q_ready, q_free, pdst_free[2];
-  uint64_t v_full[kNV], v_empty[kNV];
-  uint64_t p_full[2], p_consumed[2];
+  uint64_t q_ready, q_free, msg_ready[kNStage], staging_free[kNStage], pdst_free[kNInbox];
+  uint64_t p_full[kNInbox], p_consumed[kNInbox];
   uint64_t drain, job_full, corr_done, epi_done, final_bar;
   uint32_t tmem_base;
   volatile int abort;
@@ -103,6 +112,7 @@ struct Shared {
 
 struct Item {
   int b, t, s, P, nb;
+  int rot;  // first key block of this tile's sweep (see decode)
   int64_t k0;
   bool bad;
 };
@@ -121,7 +131,17 @@ __device__ __forceinline__ Item decode(const TcParams& p, int item) {
   int64_t k1 = it.k0 + p.chunk < kv_len ? it.k0 + p.chunk : kv_len;
   if (it.bad) k1 = it.k0;
   it.nb = k1 > it.k0 ? (int)((k1 - it.k0 + kBN - 1) / kBN) : 0;
+  // The row tiles of one sequence run at the same time on neighbouring clusters; each
+  // starts its sweep over the key blocks at a different block so that they do not all
+  // request the same cache lines at once (the softmax is independent of block order).
+  it.rot = it.nb > 0 ? (int)(((int64_t)it.t * it.nb) / p.tiles_per_seq) : 0;
   return it;
+}
+
+// Key block visited at step j of the tile's sweep.
+__device__ __forceinline__ int sweep_block(const Item& it, int j) {
+  const int jj = j + it.rot;
+  return jj >= it.nb ? jj - it.nb : jj;
 }
 
 __device__ __forceinline__ void raise_abort(Shared& sh, int32_t* status, int code) {
@@ -158,6 +178,30 @@ __device__ __forceinline__ int64_t block_row0(const TcParams& p, const Item& it,
   return (int64_t)it.b * p.kv_stride_b + key0;
 }
 
+// Visibility of keys key0 .. key0+63 for a row whose node has ancestor bitset `anc`: bit k
+// set iff key0 + k < k1 and (key0 + k is a prefix key, or the tree node key0 + k - P is an
+// ancestor-or-self of the row's node).
+__device__ __forceinline__ uint64_t block_vis(int64_t key0, int64_t P, int64_t k1, uint64_t anc) {
+  const int64_t np = P - key0;
+  const uint64_t pm = np >= 64 ? ~0ull : (np <= 0 ? 0ull : ((1ull << np) - 1));
+  const int64_t sh = key0 - P;
+  const uint64_t tm = sh >= 0 ? (sh >= 64 ? 0ull : (anc >> sh)) : (-sh >= 64 ? 0ull : (anc << (-sh)));
+  const int64_t nr = k1 - key0;
+  const uint64_t rm = nr >= 64 ? ~0ull : (nr <= 0 ? 0ull : ((1ull << nr) - 1));
+  return (pm | tm) & rm;
+}
+
+__device__ __forceinline__ float max64(const float* t) {
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = fmaxf(fmaxf(t[4 * i], t[4 * i + 1]), fmaxf(t[4 * i + 2], t[4 * i + 3]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
+  return a[0];
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -169,59 +213,66 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUtensorMap* map_kpe,
                        Shared& sh, unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned char* ring = smem;
-  unsigned char* stage = smem + kNK * kChunkBytes;
+  unsigned char* lat = smem;
+  unsigned char* rope = smem + kLatBytes;
+  unsigned char* stage = rope + kNR * kChunkBytes;
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer: 9 chunks per key block -------------------------
+    // ---------------- TMA producer: the rope chunk of each key block ----------------
+    // (the latent chunks arrive by multicast from rank 1's producer)
     if (lane == 0) {
-      prefetch_tensormap(map_ckv);
       prefetch_tensormap(map_kpe);
-      uint32_t kc = 0;
+      uint32_t kb = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
-        for (int j = 0; j < it.nb; ++j) {
-          const int row0 = (int)block_row0(p, it, j);
-          for (int c = 0; c < kKChunks; ++c, ++kc) {
-            const uint32_t slot = kc % kNK;
-            if (!wait_bar(sh, &sh.k_empty[slot], ((kc / kNK) & 1) ^ 1, p.status)) return;
-            mbar_arrive_expect_tx(&sh.k_full[slot], kChunkBytes);
-            if (c < 8)
-              tma_load_2d(ring + slot * kChunkBytes, map_ckv, 64 * c, row0, &sh.k_full[slot]);
-            else
-              tma_load_2d(ring + slot * kChunkBytes, map_kpe, 0, row0, &sh.k_full[slot]);
-          }
+        for (int j = 0; j < it.nb; ++j, ++kb) {
+          const int row0 = (int)block_row0(p, it, sweep_block(it, j));
+          const uint32_t st = kb % kNR;
+          if (!wait_bar(sh, &sh.rope_empty[st], ((kb / kNR) & 1) ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.rope_full[st], kChunkBytes);
+          tma_load_2d(rope + st * kChunkBytes, map_kpe, 0, row0, &sh.rope_full[st]);
         }
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: S = Q K^T -----------------------------------------
     if (lane == 0) {
-      uint32_t kc = 0, sc = 0, qc = 0;
+      uint32_t kb = 0, sc = 0, qc = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
         if (it.nb == 0) continue;
         if (!wait_bar(sh, &sh.q_ready, qc & 1, p.status)) break;
         ++qc;
         tc_fence_after();
-        for (int j = 0; j < it.nb && !sh.abort; ++j, ++sc) {
+        for (int j = 0; j < it.nb && !sh.abort; ++j, ++sc, ++kb) {
           const uint32_t sb = sc & 1;
           if (!wait_bar(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
-          tc_fence_after();
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
-          for (int c = 0; c < kKChunks; ++c, ++kc) {
-            const uint32_t slot = kc % kNK;
-            if (!wait_bar(sh, &sh.k_full[slot], (kc / kNK) & 1, p.status)) break;
+          bool ok = true;
+          for (int h = 0; h < 2 && ok; ++h) {
+            const uint32_t u = 2 * kb + h, st = u % kNL;
+            if (!wait_bar(sh, &sh.lat_full[st], (u / kNL) & 1, p.status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = smem_u32(ring + slot * kChunkBytes);
+            const uint32_t sa = smem_u32(lat + st * kHalf);
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(d, tmem + kTmQ + 32 * c + 8 * kk, smem_desc(sa + 32 * kk, 16, 1024, 2),
-                     kIdescQK, (c | kk) != 0);
-            mma_commit(&sh.k_empty[slot]);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(d, tmem + kTmQ + 32 * (4 * h + c) + 8 * kk,
+                       smem_desc(sa + c * kChunkBytes + 32 * kk, 16, 1024, 2), kIdescQK,
+                       (h | c | kk) != 0);
+            mma_commit(&sh.lat_consumed[st]);
           }
+          const uint32_t rs = kb % kNR;
+          if (!ok || !wait_bar(sh, &sh.rope_full[rs], (kb / kNR) & 1, p.status)) break;
+          tc_fence_after();
+          const uint32_t ra = smem_u32(rope + rs * kChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(d, tmem + kTmQ + 32 * 8 + 8 * kk, smem_desc(ra + 32 * kk, 16, 1024, 2),
+                   kIdescQK, 1);
+          mma_commit(&sh.rope_empty[rs]);
           mma_commit(&sh.s_full[sb]);
         }
         mma_commit(&sh.q_free);
@@ -229,13 +280,66 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
       mma_commit(&sh.final_bar);
       wait_bar(sh, &sh.final_bar, 0, p.status);
     }
+  } else if (warp == 3) {
+    // ---------------- latent-ring helper: once this CTA has read a stage, re-arm it and
+    // tell rank 1's producer that the stage may be refilled ------------------------------
+    if (lane == 0) {
+      const uint32_t peer = cluster_rank() ^ 1u;
+      uint32_t u = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        for (int j = 0; j < 2 * it.nb; ++j, ++u) {
+          const uint32_t st = u % kNL;
+          if (!wait_bar(sh, &sh.lat_consumed[st], (u / kNL) & 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.lat_full[st], kHalf);
+          mbar_arrive_remote(map_to_rank(smem_u32(&sh.lat_empty[st]), peer));
+        }
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- sender: staging buffer -> peer inbox, one bulk copy per block --
+    const uint32_t peer = cluster_rank() ^ 1u;
+    unsigned char* peer_inbox_local = smem + kLatBytes;  // same offset in the peer
+    uint32_t mc = 0;
+    bool live = true;
+    for (int item = cid; item < p.n_items && live && !sh.abort; item += ncl) {
+      const Item it = decode(p, item);
+      for (int j = 0; j < it.nb; ++j, ++mc) {
+        const uint32_t sbuf = mc % kNStage, ib = mc % kNInbox;
+        if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.msg_ready[sbuf], (mc / kNStage) & 1, p.status))) {
+          live = false;
+          break;
+        }
+        unsigned char* msg = stage + sbuf * kMsgStride;
+        const float* alpha = reinterpret_cast<const float*>(msg + kMsgAlpha);
+        bool resc = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) resc |= alpha[lane * 4 + q] != 1.f;
+        resc = __any_sync(0xffffffffu, resc);
+        if (lane == 0) {
+          const uint32_t flags = (j == 0 ? kFlagFirst : 0u) | (j == it.nb - 1 ? kFlagFinal : 0u) |
+                                 ((resc && j > 0) ? kFlagRescale : 0u);
+          *reinterpret_cast<volatile uint32_t*>(msg + kMsgHdr) = flags;
+          fence_proxy_async_smem();
+          if (wait_bar(sh, &sh.pdst_free[ib], ((mc / kNInbox) & 1) ^ 1, p.status)) {
+            const uint32_t dst = map_to_rank(smem_u32(peer_inbox_local + ib * kMsgStride), peer);
+            const uint32_t bar = map_to_rank(smem_u32(&sh.p_full[ib]), peer);
+            bulk_copy_to_cluster(dst, msg, kMsgBytes, bar);
+            bulk_commit();
+            bulk_wait_read<0>();
+          }
+          mbar_arrive(&sh.staging_free[sbuf]);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   } else if (warp >= 4) {
     // ---------------- softmax warpgroup: thread r owns tile row r ------------------
     const int wq = warp - 4;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t peer = cluster_rank() ^ 1u;
-    unsigned char* peer_inbox_local = smem + kNV * kVStage;  // same offset in the peer
+    const float c = p.scale_log2;
     uint32_t sc = 0, qc = 0, mc = 0;
     for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
       const Item it = decode(p, item);
@@ -248,14 +352,28 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
         if (vrow) *lse_dst = -INFINITY;
         continue;
       }
+      {
+        // warm L2 with the next tile's queries while this tile runs
+        const int nxt = item + ncl;
+        if (nxt < p.n_items) {
+          const Item in = decode(p, nxt);
+          const int nrow = in.t * kRows + r;
+          if (in.nb > 0 && nrow < p.Q * p.H) {
+            const int64_t ng = (int64_t)in.b * p.Q * p.H + nrow;
+            const char* qlp = reinterpret_cast<const char*>(p.q_latent + ng * kDL);
+#pragma unroll
+            for (int l128 = 0; l128 < 8; ++l128) prefetch_l2(qlp + 128 * l128);
+            prefetch_l2(p.q_pe + ng * kDR);
+          }
+        }
+      }
       const uint64_t anc = vrow ? p.anc[(int64_t)it.b * p.Q + trow / p.H] : 0ull;
       const int64_t kv_end = (int64_t)it.P + p.Q;
       const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
 
       // ---- queries of this row into TMEM columns [0, 288) ----
-      // (every wait of the warpgroup ends in a barrier that agrees on its outcome, so that
-      // no thread is left waiting in a barrier for one that gave up)
-      if (!named_sync_and(1, 128, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) break;
+      // (each warp agrees on the outcome of a wait before its warp-collective TMEM ops)
+      if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) break;
       ++qc;
       tc_fence_after();
       {
@@ -266,11 +384,11 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
           uint32_t w[3][32];
 #pragma unroll
           for (int cc = 0; cc < 3; ++cc) {
-            const int c = c0 + cc;
+            const int ch = c0 + cc;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               uint4 v = make_uint4(0, 0, 0, 0);
-              if (vrow) v = c < 8 ? __ldg(ql + 8 * c + e) : __ldg(qr + e);
+              if (vrow) v = ch < 8 ? __ldg(ql + 8 * ch + e) : __ldg(qr + e);
               w[cc][4 * e + 0] = v.x;
               w[cc][4 * e + 1] = v.y;
               w[cc][4 * e + 2] = v.z;
@@ -289,82 +407,96 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.nb; ++j, ++sc, ++mc) {
         const uint32_t sb = sc & 1;
-        if (!named_sync_and(1, 128, wait_bar(sh, &sh.s_full[sb], (sc >> 1) & 1, p.status))) break;
+        if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.s_full[sb], (sc >> 1) & 1, p.status))) break;
         tc_fence_after();
-        uint32_t sr[64];
-        tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0), sr);
-        tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0) + 32, sr + 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&sh.s_empty[sb]);
+        float t[64];
+        {
+          uint32_t sr[64];
+          tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0), sr);
+          tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0) + 32, sr + 32);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&sh.s_empty[sb]);
+#pragma unroll
+          for (int k = 0; k < 64; ++k) t[k] = __uint_as_float(sr[k]);
+        }
+        const int64_t key0 = it.k0 + (int64_t)sweep_block(it, j) * kBN;
+        const uint64_t vis =
+            (key0 + kBN > it.P || key0 + kBN > k1) ? block_vis(key0, it.P, k1, anc) : ~0ull;
 
-        float x[64];
-        const int64_t key0 = it.k0 + (int64_t)j * kBN;
-        const bool need_mask = key0 + kBN > it.P || key0 + kBN > k1;
-        float bm = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          float v = __uint_as_float(sr[k]) * p.scale_log2;
-          if (need_mask) {
-            const int64_t key = key0 + k;
-            const bool vis = key < k1 && (key < it.P || ((anc >> (int)(key - it.P)) & 1ull));
-            v = vis ? v : -INFINITY;
-          }
-          x[k] = v;
-          bm = fmaxf(bm, v);
-        }
         float alpha = 1.f;
-        bool resc = false;
-        if (bm > m + kRescaleThreshold) {
-          alpha = exp2f(m - bm);
-          resc = l > 0.f;
-          m = bm;
-        }
-        float sum = 0.f;
         uint32_t pk[32];
+        float sum = 0.f;
+        if (m != -INFINITY) {
+          // t = score*c - m (masked keys -inf); exponentiate against the current max
+          // while the block max is reduced; only a max that grew by more than 2^8
+          // (rare) makes the block go round again with the new max.
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const float p0 = x[k] == -INFINITY ? 0.f : exp2f(x[k] - m);
-          const float p1 = x[k + 1] == -INFINITY ? 0.f : exp2f(x[k + 1] - m);
-          sum += p0 + p1;
-          pk[k >> 1] = pack_bf16(p0, p1);
+          for (int k = 0; k < 64; ++k) {
+            const float v = fmaf(t[k], c, -m);
+            t[k] = ((vis >> k) & 1ull) ? v : -INFINITY;
+          }
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            const float p0 = ex2(t[k]), p1 = ex2(t[k + 1]);
+            s4[(k >> 1) & 3] += p0 + p1;
+            pk[k >> 1] = pack_bf16(p0, p1);
+          }
+          const float bmt = max64(t);
+          if (bmt > kRescaleThreshold) {
+            alpha = ex2(-bmt);
+            m += bmt;
+            s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
+#pragma unroll
+            for (int k = 0; k < 64; k += 2) {
+              const float p0 = ex2(t[k] - bmt), p1 = ex2(t[k + 1] - bmt);
+              s4[(k >> 1) & 3] += p0 + p1;
+              pk[k >> 1] = pack_bf16(p0, p1);
+            }
+          }
+          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        } else {
+          // first block with visible keys for this row: the max comes first
+#pragma unroll
+          for (int k = 0; k < 64; ++k) t[k] = ((vis >> k) & 1ull) ? t[k] * c : -INFINITY;
+          const float bm = max64(t);
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+          if (bm != -INFINITY) {
+            m = bm;  // l == 0 so far: nothing accumulated to rescale (alpha stays 1)
+#pragma unroll
+            for (int k = 0; k < 64; k += 2) {
+              const float p0 = ex2(t[k] - m), p1 = ex2(t[k + 1] - m);
+              s4[(k >> 1) & 3] += p0 + p1;
+              pk[k >> 1] = pack_bf16(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) pk[k] = 0u;
+          }
+          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
         l = l * alpha + sum;
 
-        // ---- ship P, alpha (and the row sums on the last block) to rank 1 ----
-        const uint32_t pb = mc & 1;
-        unsigned char* msg = stage + pb * kMsgStride;
-        if (r == 0) bulk_wait_read<1>();
-        named_sync(1, 128);
-        {
-          unsigned char* rowp = msg + (r >> 3) * 1024 + (r & 7) * 128;
+        // ---- P (bf16, swizzled K-major), alpha and, last, the row sum into staging ----
+        const uint32_t sbuf = mc % kNStage;
+        if (!__all_sync(0xffffffffu,
+                        wait_bar(sh, &sh.staging_free[sbuf], ((mc / kNStage) & 1) ^ 1, p.status)))
+          break;
+        unsigned char* msg = stage + sbuf * kMsgStride;
+        unsigned char* rowp = msg + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          reinterpret_cast<float*>(msg + kMsgAlpha)[r] = alpha;
-          if (j == it.nb - 1) reinterpret_cast<float*>(msg + kMsgL)[r] = l;
-        }
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        reinterpret_cast<float*>(msg + kMsgAlpha)[r] = alpha;
+        if (j == it.nb - 1) reinterpret_cast<float*>(msg + kMsgL)[r] = l;
         fence_proxy_async_smem();
-        const bool any_resc = named_sync_or(1, 128, resc);
-        if (r == 0) {
-          uint32_t flags = (j == 0 ? kFlagFirst : 0u) | (j == it.nb - 1 ? kFlagFinal : 0u) |
-                           ((any_resc && j > 0) ? kFlagRescale : 0u);
-          *reinterpret_cast<volatile uint32_t*>(msg + kMsgHdr) = flags;
-          fence_proxy_async_smem();
-          if (wait_bar(sh, &sh.pdst_free[pb], ((mc >> 1) & 1) ^ 1, p.status)) {
-            const uint32_t dst = map_to_rank(smem_u32(peer_inbox_local + pb * kMsgStride), peer);
-            const uint32_t bar = map_to_rank(smem_u32(&sh.p_full[pb]), peer);
-            bulk_copy_to_cluster(dst, msg, kMsgBytes, bar);
-            bulk_commit();
-          }
-        }
-        __syncwarp();
+        mbar_arrive(&sh.msg_ready[sbuf]);
       }
       if (vrow && !sh.abort)
         *lse_dst = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
-    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 }
 
@@ -374,28 +506,29 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
 __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh,
                        unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned char* vring = smem;
-  unsigned char* inbox = smem + kNV * kVStage;
+  unsigned char* lat = smem;
+  unsigned char* inbox = smem + kLatBytes;
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer: latent chunks as V -----------------------------
+    // ---------------- TMA producer: latent halves, multicast to both CTAs ------------
     if (lane == 0) {
       prefetch_tensormap(map_ckv);
-      uint32_t vc = 0;
+      uint32_t u = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
         for (int j = 0; j < it.nb; ++j) {
-          const int row0 = (int)block_row0(p, it, j);
-          for (int h = 0; h < 2; ++h, ++vc) {
-            const uint32_t st = vc % kNV;
-            if (!wait_bar(sh, &sh.v_empty[st], ((vc / kNV) & 1) ^ 1, p.status)) return;
-            mbar_arrive_expect_tx(&sh.v_full[st], kVStage);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tma_load_2d(vring + st * kVStage + q * kChunkBytes, map_ckv, 256 * h + 64 * q,
-                          row0, &sh.v_full[st]);
+          const int row0 = (int)block_row0(p, it, sweep_block(it, j));
+          for (int h = 0; h < 2; ++h, ++u) {
+            const uint32_t st = u % kNL;
+            // this CTA finished the stage's previous use ...
+            if (!wait_bar(sh, &sh.lat_consumed[st], ((u / kNL) & 1) ^ 1, p.status)) return;
+            if (u >= (uint32_t)kNL) mbar_arrive_expect_tx(&sh.lat_full[st], kHalf);
+            // ... and so did rank 0 (which has re-armed its own barrier)
+            if (!wait_bar(sh, &sh.lat_empty[st], ((u / kNL) & 1) ^ 1, p.status)) return;
+            tma_load_3d_multicast(lat + st * kHalf, map_ckv, 0, row0, 4 * h, &sh.lat_full[st],
+                                  (uint16_t)0x3);
           }
         }
       }
@@ -412,9 +545,9 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
         uint32_t last_pb = 0;
         bool ok = true;
         for (int j = 0; j < it.nb && ok; ++j, ++mc) {
-          const uint32_t pb = mc & 1;
+          const uint32_t pb = mc % kNInbox;
           last_pb = pb;
-          if (!wait_bar(sh, &sh.p_full[pb], (mc >> 1) & 1, p.status)) { ok = false; break; }
+          if (!wait_bar(sh, &sh.p_full[pb], (mc / kNInbox) & 1, p.status)) { ok = false; break; }
           const uint32_t flags =
               *reinterpret_cast<volatile uint32_t*>(inbox + pb * kMsgStride + kMsgHdr);
           if (flags & kFlagRescale) {
@@ -430,15 +563,15 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
           }
           const uint32_t pa = smem_u32(inbox + pb * kMsgStride);
           for (int h = 0; h < 2; ++h, ++vc) {
-            const uint32_t st = vc % kNV;
-            if (!wait_bar(sh, &sh.v_full[st], (vc / kNV) & 1, p.status)) { ok = false; break; }
+            const uint32_t st = vc % kNL;
+            if (!wait_bar(sh, &sh.lat_full[st], (vc / kNL) & 1, p.status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t va = smem_u32(vring + st * kVStage);
+            const uint32_t va = smem_u32(lat + st * kHalf);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(tmem + 256 * h, smem_desc(pa + 32 * kk, 16, 1024, 2),
                      smem_desc(va + 2048 * kk, 8192, 1024, 2), kIdescPV, (j | kk) != 0);
-            mma_commit(&sh.v_empty[st]);
+            mma_commit(&sh.lat_consumed[st]);
           }
           mma_commit(&sh.p_consumed[pb]);
         }
@@ -466,8 +599,8 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
         const Item it = decode(p, item);
         if (it.nb == 0) continue;
         for (int j = 0; j < it.nb; ++j, ++mc) {
-          const uint32_t pb = mc & 1;
-          if (!wait_bar(sh, &sh.p_consumed[pb], (mc >> 1) & 1, p.status)) return;
+          const uint32_t pb = mc % kNInbox;
+          if (!wait_bar(sh, &sh.p_consumed[pb], (mc / kNInbox) & 1, p.status)) return;
           if (j == it.nb - 1 && !wait_bar(sh, &sh.epi_done, ic & 1, p.status)) return;
           mbar_arrive_expect_tx(&sh.p_full[pb], kMsgBytes);
           mbar_arrive_remote(map_to_rank(smem_u32(&sh.pdst_free[pb]), peer));
@@ -557,17 +690,24 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNK; ++i) {
-      mbar_init(&sh.k_full[i], 1);
-      mbar_init(&sh.k_empty[i], 1);
+    for (int i = 0; i < kNL; ++i) {
+      mbar_init(&sh.lat_full[i], 1);
+      mbar_init(&sh.lat_consumed[i], 1);
+      mbar_init(&sh.lat_empty[i], 1);
     }
-    for (int i = 0; i < kNV; ++i) {
-      mbar_init(&sh.v_full[i], 1);
-      mbar_init(&sh.v_empty[i], 1);
+    for (int i = 0; i < kNR; ++i) {
+      mbar_init(&sh.rope_full[i], 1);
+      mbar_init(&sh.rope_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 128);
+    }
+    for (int i = 0; i < kNStage; ++i) {
+      mbar_init(&sh.msg_ready[i], 128);
+      mbar_init(&sh.staging_free[i], 1);
+    }
+    for (int i = 0; i < kNInbox; ++i) {
       mbar_init(&sh.pdst_free[i], 1);
       mbar_init(&sh.p_full[i], 1);
       mbar_init(&sh.p_consumed[i], 1);
@@ -582,10 +722,11 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
     sh.abort = 0;
     sh.job_type = 0;
     sh.job_buf = 0;
+    // both CTAs start with every latent stage armed for its first multicast
+    for (int i = 0; i < kNL; ++i) mbar_arrive_expect_tx(&sh.lat_full[i], kHalf);
     if (rank == 1) {
-      // both inbox buffers start armed for the first two messages
-      mbar_arrive_expect_tx(&sh.p_full[0], kMsgBytes);
-      mbar_arrive_expect_tx(&sh.p_full[1], kMsgBytes);
+      // every inbox buffer starts armed for its first message
+      for (int i = 0; i < kNInbox; ++i) mbar_arrive_expect_tx(&sh.p_full[i], kMsgBytes);
     }
     fence_mbar_init();
   }
@@ -626,6 +767,19 @@ bool get_encode() {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   return g_encode != nullptr;
+}
+
+// Latent rows viewed as [64 elements][rows][8 chunks of 64 elements]: one box is 4 chunks
+// of 64 rows, landing chunk-major in shared memory as four 128-byte-swizzled 8 KB tiles.
+bool make_map_latent(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes) {
+  cuuint64_t dims[3] = {64, rows, kDL / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, 64, 4};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
@@ -716,7 +870,7 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   if (!get_encode()) return cudaErrorNotSupported;
   if (max_clusters() <= 0) return cudaErrorNotSupported;
   CUtensorMap mc, mk;
-  if (!make_map(&mc, a->c_kv, kDL, (uint64_t)a->cache.num_rows, (uint64_t)a->ckv_row_stride * 2))
+  if (!make_map_latent(&mc, a->c_kv, (uint64_t)a->cache.num_rows, (uint64_t)a->ckv_row_stride * 2))
     return cudaErrorInvalidValue;
   if (!make_map(&mk, a->k_pe, kDR, (uint64_t)a->cache.num_rows, (uint64_t)a->kpe_row_stride * 2))
     return cudaErrorInvalidValue;

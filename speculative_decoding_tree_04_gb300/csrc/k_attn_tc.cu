@@ -13,9 +13,9 @@
 // tensor memory, leaving no room for S.  So each tile is served by a cluster of two CTAs
 // on two SMs that split the two contractions between them:
 //
-//   rank 0 ("S side"): holds the tile's queries in TMEM (A operand of QK^T), streams each
-//     64-key block through a two-stage TMA ring (two 3-D boxes of 4 latent chunks each plus
-//     the rope chunk: few, large requests keep the TMA engine busy), computes S into one of two TMEM
+//   rank 0 ("S side"): holds the tile's queries in TMEM (A operand of QK^T), receives each
+//     64-key block's latent rows (two 3-D boxes of 4 chunks, loaded for it by rank 1's TMA
+//     engine) and loads the rope chunk itself, computes S into one of two TMEM
 //     buffers, runs the masked online softmax (lazy rescaling: the running max only moves
 //     when it grows by more than 2^8), and ships each block's P (bf16, in the swizzled
 //     K-major layout the MMA reads), the per-row rescale factors and, at the end, the row
@@ -56,19 +56,21 @@ constexpr int kDL = 512, kDR = 64, kBN = 64, kRows = 128;
 constexpr int kChunkBytes = kBN * 128;          // 64 keys x 64 bf16
 constexpr int kKChunks = 9;                     // 8 latent + 1 rope chunk per key block
 constexpr int kHalf = 4 * kChunkBytes;          // 4 latent chunks: one 3-D TMA box
-constexpr int kNL = 4;                          // latent ring stages (half key blocks)
+constexpr int kNLS = 5;                         // S-side latent ring stages (half key blocks)
+constexpr int kNLO = 4;                         // O-side latent ring stages
 constexpr int kNR = 2;                          // S-side rope ring stages
 constexpr int kMsgAlpha = 16384, kMsgL = 16896, kMsgHdr = 17408, kMsgBytes = 17424;
 constexpr int kMsgStride = 18432;
 constexpr int kNStage = 2;                      // S-side staging buffers
 constexpr int kNInbox = 4;                      // O-side inbox buffers
 constexpr int kThreads = 256;
-// Shared memory, from offset 0 in both CTAs: the latent ring (multicast by rank 1 into
-// both CTAs at the same offset), then on rank 0 the rope ring and the staging buffers,
-// on rank 1 the inbox.
-constexpr int kLatBytes = kNL * kHalf;
-constexpr int kSideA = kLatBytes + kNR * kChunkBytes + kNStage * kMsgStride;
-constexpr int kSideB = kLatBytes + kNInbox * kMsgStride;
+// Shared memory, from offset 0 in each CTA: its own latent ring (both are filled by rank
+// 1's TMA engine: rank 0's through a multicast addressed to rank 0 only), then on rank 0
+// the rope ring and the staging buffers, on rank 1 the inbox.
+constexpr int kLatS = kNLS * kHalf;
+constexpr int kLatO = kNLO * kHalf;
+constexpr int kSideA = kLatS + kNR * kChunkBytes + kNStage * kMsgStride;
+constexpr int kSideB = kLatO + kNInbox * kMsgStride;
 constexpr int kSmemBytes = (kSideA > kSideB ? kSideA : kSideB) + 1024;
 constexpr uint32_t kTmQ = 0, kTmS0 = 288, kTmS1 = 352;       // S-side TMEM columns
 constexpr uint32_t kFlagFirst = 1, kFlagRescale = 2, kFlagFinal = 4;
@@ -99,7 +101,8 @@ struct TcParams {
 };
 
 struct Shared {
-  uint64_t lat_full[kNL], lat_consumed[kNL], lat_empty[kNL];
+  uint64_t slat_full[kNLS], slat_consumed[kNLS], slat_empty[kNLS];
+  uint64_t olat_full[kNLO], olat_consumed[kNLO];
   uint64_t rope_full[kNR], rope_empty[kNR];
   uint64_t s_full[2], s_empty[2];
   uint64_t q_ready, q_free, msg_ready[kNStage], staging_free[kNStage], pdst_free[kNInbox];
@@ -117,7 +120,7 @@ struct Item {
   bool bad;
 };
 
-__device__ __forceinline__ Item decode(const TcParams& p, int item) {
+__device__ __noinline__ Item decode(const TcParams& p, int item) {
   Item it;
   it.t = item % p.tiles_per_seq;
   const int bs = item / p.tiles_per_seq;
@@ -154,11 +157,10 @@ __device__ __forceinline__ void raise_abort(Shared& sh, int32_t* status, int cod
   }
 }
 
-// Bounded wait on phase `parity` of a local mbarrier.
-__device__ __forceinline__ bool wait_bar(Shared& sh, uint64_t* bar, uint32_t parity,
-                                         int32_t* status) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+// Bounded wait on phase `parity` of a local mbarrier: one inline probe, then an out-of-line
+// polling loop with a wall-clock deadline (kept out of line to keep hot loops small).
+__device__ __noinline__ bool wait_bar_slow(Shared& sh, uint32_t a, uint32_t parity,
+                                           int32_t* status) {
   const uint64_t t0 = globaltimer();
   for (;;) {
 #pragma unroll 1
@@ -170,6 +172,13 @@ __device__ __forceinline__ bool wait_bar(Shared& sh, uint64_t* bar, uint32_t par
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(Shared& sh, uint64_t* bar, uint32_t parity,
+                                         int32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  return wait_bar_slow(sh, a, parity, status);
 }
 
 __device__ __forceinline__ int64_t block_row0(const TcParams& p, const Item& it, int j) {
@@ -214,7 +223,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
                        Shared& sh, unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* lat = smem;
-  unsigned char* rope = smem + kLatBytes;
+  unsigned char* rope = smem + kLatS;
   unsigned char* stage = rope + kNR * kChunkBytes;
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const uint32_t tmem = sh.tmem_base;
@@ -249,12 +258,12 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
         for (int j = 0; j < it.nb && !sh.abort; ++j, ++sc, ++kb) {
           const uint32_t sb = sc & 1;
           if (!wait_bar(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
+          tc_fence_after();  // the softmax warps' TMEM reads of this S buffer come first
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
           bool ok = true;
           for (int h = 0; h < 2 && ok; ++h) {
-            const uint32_t u = 2 * kb + h, st = u % kNL;
-            if (!wait_bar(sh, &sh.lat_full[st], (u / kNL) & 1, p.status)) { ok = false; break; }
-            tc_fence_after();
+            const uint32_t u = 2 * kb + h, st = u % kNLS;
+            if (!wait_bar(sh, &sh.slat_full[st], (u / kNLS) & 1, p.status)) { ok = false; break; }
             const uint32_t sa = smem_u32(lat + st * kHalf);
             for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -262,11 +271,10 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
                 mma_ts(d, tmem + kTmQ + 32 * (4 * h + c) + 8 * kk,
                        smem_desc(sa + c * kChunkBytes + 32 * kk, 16, 1024, 2), kIdescQK,
                        (h | c | kk) != 0);
-            mma_commit(&sh.lat_consumed[st]);
+            mma_commit(&sh.slat_consumed[st]);
           }
           const uint32_t rs = kb % kNR;
           if (!ok || !wait_bar(sh, &sh.rope_full[rs], (kb / kNR) & 1, p.status)) break;
-          tc_fence_after();
           const uint32_t ra = smem_u32(rope + rs * kChunkBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -282,24 +290,24 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
     }
   } else if (warp == 3) {
     // ---------------- latent-ring helper: once this CTA has read a stage, re-arm it and
-    // tell rank 1's producer that the stage may be refilled ------------------------------
+    // tell rank 1's producer for this ring that the stage may be refilled ---------------
     if (lane == 0) {
       const uint32_t peer = cluster_rank() ^ 1u;
       uint32_t u = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
         for (int j = 0; j < 2 * it.nb; ++j, ++u) {
-          const uint32_t st = u % kNL;
-          if (!wait_bar(sh, &sh.lat_consumed[st], (u / kNL) & 1, p.status)) return;
-          mbar_arrive_expect_tx(&sh.lat_full[st], kHalf);
-          mbar_arrive_remote(map_to_rank(smem_u32(&sh.lat_empty[st]), peer));
+          const uint32_t st = u % kNLS;
+          if (!wait_bar(sh, &sh.slat_consumed[st], (u / kNLS) & 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.slat_full[st], kHalf);
+          mbar_arrive_remote(map_to_rank(smem_u32(&sh.slat_empty[st]), peer));
         }
       }
     }
   } else if (warp == 2) {
     // ---------------- sender: staging buffer -> peer inbox, one bulk copy per block --
     const uint32_t peer = cluster_rank() ^ 1u;
-    unsigned char* peer_inbox_local = smem + kLatBytes;  // same offset in the peer
+    unsigned char* peer_inbox_local = smem + kLatO;  // same offset in the peer
     uint32_t mc = 0;
     bool live = true;
     for (int item = cid; item < p.n_items && live && !sh.abort; item += ncl) {
@@ -424,58 +432,27 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
         const uint64_t vis =
             (key0 + kBN > it.P || key0 + kBN > k1) ? block_vis(key0, it.P, k1, anc) : ~0ull;
 
+        // scaled scores (masked keys -inf), block max, then one exponentiation pass.  The
+        // running max only moves when the block max exceeds it by more than 2^8 (lazy
+        // rescaling); a row's first visible keys set it.
+#pragma unroll
+        for (int k = 0; k < 64; ++k) t[k] = ((vis >> k) & 1ull) ? t[k] * c : -INFINITY;
+        const float bm = max64(t);
         float alpha = 1.f;
-        uint32_t pk[32];
-        float sum = 0.f;
-        if (m != -INFINITY) {
-          // t = score*c - m (masked keys -inf); exponentiate against the current max
-          // while the block max is reduced; only a max that grew by more than 2^8
-          // (rare) makes the block go round again with the new max.
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const float v = fmaf(t[k], c, -m);
-            t[k] = ((vis >> k) & 1ull) ? v : -INFINITY;
-          }
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int k = 0; k < 64; k += 2) {
-            const float p0 = ex2(t[k]), p1 = ex2(t[k + 1]);
-            s4[(k >> 1) & 3] += p0 + p1;
-            pk[k >> 1] = pack_bf16(p0, p1);
-          }
-          const float bmt = max64(t);
-          if (bmt > kRescaleThreshold) {
-            alpha = ex2(-bmt);
-            m += bmt;
-            s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
-#pragma unroll
-            for (int k = 0; k < 64; k += 2) {
-              const float p0 = ex2(t[k] - bmt), p1 = ex2(t[k + 1] - bmt);
-              s4[(k >> 1) & 3] += p0 + p1;
-              pk[k >> 1] = pack_bf16(p0, p1);
-            }
-          }
-          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        } else {
-          // first block with visible keys for this row: the max comes first
-#pragma unroll
-          for (int k = 0; k < 64; ++k) t[k] = ((vis >> k) & 1ull) ? t[k] * c : -INFINITY;
-          const float bm = max64(t);
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-          if (bm != -INFINITY) {
-            m = bm;  // l == 0 so far: nothing accumulated to rescale (alpha stays 1)
-#pragma unroll
-            for (int k = 0; k < 64; k += 2) {
-              const float p0 = ex2(t[k] - m), p1 = ex2(t[k + 1] - m);
-              s4[(k >> 1) & 3] += p0 + p1;
-              pk[k >> 1] = pack_bf16(p0, p1);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) pk[k] = 0u;
-          }
-          sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        if (bm > m + kRescaleThreshold) {  // also true for the first visible keys (m = -inf)
+          if (l > 0.f) alpha = ex2(m - bm);
+          m = bm;
         }
+        const float mm = m == -INFINITY ? 0.f : m;  // all keys so far masked: every p is 0
+        uint32_t pk[32];
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const float p0 = ex2(t[k] - mm), p1 = ex2(t[k + 1] - mm);
+          s4[(k >> 1) & 3] += p0 + p1;
+          pk[k >> 1] = pack_bf16(p0, p1);
+        }
+        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         l = l * alpha + sum;
 
         // ---- P (bf16, swizzled K-major), alpha and, last, the row sum into staging ----
@@ -507,12 +484,13 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
                        unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* lat = smem;
-  unsigned char* inbox = smem + kLatBytes;
+  unsigned char* inbox = smem + kLatO;
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer: latent halves, multicast to both CTAs ------------
+    // ---------------- TMA producer for rank 0's latent ring (multicast addressed to rank
+    // 0 only, so this CTA's engine serves both rings) ----------------------------------
     if (lane == 0) {
       prefetch_tensormap(map_ckv);
       uint32_t u = 0;
@@ -521,14 +499,29 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
         for (int j = 0; j < it.nb; ++j) {
           const int row0 = (int)block_row0(p, it, sweep_block(it, j));
           for (int h = 0; h < 2; ++h, ++u) {
-            const uint32_t st = u % kNL;
-            // this CTA finished the stage's previous use ...
-            if (!wait_bar(sh, &sh.lat_consumed[st], ((u / kNL) & 1) ^ 1, p.status)) return;
-            if (u >= (uint32_t)kNL) mbar_arrive_expect_tx(&sh.lat_full[st], kHalf);
-            // ... and so did rank 0 (which has re-armed its own barrier)
-            if (!wait_bar(sh, &sh.lat_empty[st], ((u / kNL) & 1) ^ 1, p.status)) return;
-            tma_load_3d_multicast(lat + st * kHalf, map_ckv, 0, row0, 4 * h, &sh.lat_full[st],
-                                  (uint16_t)0x3);
+            const uint32_t st = u % kNLS;
+            // rank 0 has read the stage's previous fill and re-armed its barrier
+            if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
+            tma_load_3d_multicast(lat + st * kHalf, map_ckv, 0, row0, 4 * h, &sh.slat_full[st],
+                                  (uint16_t)0x1);
+          }
+        }
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------- TMA producer for this CTA's latent ring ---------------------------
+    if (lane == 0) {
+      prefetch_tensormap(map_ckv);
+      uint32_t u = 0;
+      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+        const Item it = decode(p, item);
+        for (int j = 0; j < it.nb; ++j) {
+          const int row0 = (int)block_row0(p, it, sweep_block(it, j));
+          for (int h = 0; h < 2; ++h, ++u) {
+            const uint32_t st = u % kNLO;
+            if (!wait_bar(sh, &sh.olat_consumed[st], ((u / kNLO) & 1) ^ 1, p.status)) return;
+            mbar_arrive_expect_tx(&sh.olat_full[st], kHalf);
+            tma_load_3d(lat + st * kHalf, map_ckv, 0, row0, 4 * h, &sh.olat_full[st]);
           }
         }
       }
@@ -563,15 +556,14 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
           }
           const uint32_t pa = smem_u32(inbox + pb * kMsgStride);
           for (int h = 0; h < 2; ++h, ++vc) {
-            const uint32_t st = vc % kNL;
-            if (!wait_bar(sh, &sh.lat_full[st], (vc / kNL) & 1, p.status)) { ok = false; break; }
-            tc_fence_after();
+            const uint32_t st = vc % kNLO;
+            if (!wait_bar(sh, &sh.olat_full[st], (vc / kNLO) & 1, p.status)) { ok = false; break; }
             const uint32_t va = smem_u32(lat + st * kHalf);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(tmem + 256 * h, smem_desc(pa + 32 * kk, 16, 1024, 2),
                      smem_desc(va + 2048 * kk, 8192, 1024, 2), kIdescPV, (j | kk) != 0);
-            mma_commit(&sh.lat_consumed[st]);
+            mma_commit(&sh.olat_consumed[st]);
           }
           mma_commit(&sh.p_consumed[pb]);
         }
@@ -690,10 +682,14 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNL; ++i) {
-      mbar_init(&sh.lat_full[i], 1);
-      mbar_init(&sh.lat_consumed[i], 1);
-      mbar_init(&sh.lat_empty[i], 1);
+    for (int i = 0; i < kNLS; ++i) {
+      mbar_init(&sh.slat_full[i], 1);
+      mbar_init(&sh.slat_consumed[i], 1);
+      mbar_init(&sh.slat_empty[i], 1);
+    }
+    for (int i = 0; i < kNLO; ++i) {
+      mbar_init(&sh.olat_full[i], 1);
+      mbar_init(&sh.olat_consumed[i], 1);
     }
     for (int i = 0; i < kNR; ++i) {
       mbar_init(&sh.rope_full[i], 1);
@@ -722,8 +718,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
     sh.abort = 0;
     sh.job_type = 0;
     sh.job_buf = 0;
-    // both CTAs start with every latent stage armed for its first multicast
-    for (int i = 0; i < kNL; ++i) mbar_arrive_expect_tx(&sh.lat_full[i], kHalf);
+    if (rank == 0) {
+      // rank 0's latent stages start armed for their first fill (issued by rank 1)
+      for (int i = 0; i < kNLS; ++i) mbar_arrive_expect_tx(&sh.slat_full[i], kHalf);
+    }
     if (rank == 1) {
       // every inbox buffer starts armed for its first message
       for (int i = 0; i < kNInbox; ++i) mbar_arrive_expect_tx(&sh.p_full[i], kMsgBytes);

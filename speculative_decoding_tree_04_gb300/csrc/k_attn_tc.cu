@@ -236,8 +236,11 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
       uint32_t kb = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
+        // the page-table lookup for the next block is issued a block ahead
+        int next_row = it.nb > 0 ? (int)block_row0(p, it, sweep_block(it, 0)) : 0;
         for (int j = 0; j < it.nb; ++j, ++kb) {
-          const int row0 = (int)block_row0(p, it, sweep_block(it, j));
+          const int row0 = next_row;
+          if (j + 1 < it.nb) next_row = (int)block_row0(p, it, sweep_block(it, j + 1));
           const uint32_t st = kb % kNR;
           if (!wait_bar(sh, &sh.rope_empty[st], ((kb / kNR) & 1) ^ 1, p.status)) return;
           mbar_arrive_expect_tx(&sh.rope_full[st], kChunkBytes);
@@ -432,25 +435,33 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
         const uint64_t vis =
             (key0 + kBN > it.P || key0 + kBN > k1) ? block_vis(key0, it.P, k1, anc) : ~0ull;
 
-        // scaled scores (masked keys -inf), block max, then one exponentiation pass.  The
-        // running max only moves when the block max exceeds it by more than 2^8 (lazy
-        // rescaling); a row's first visible keys set it.
+        // t = score*c - m (masked keys -inf), exponentiated against the current running
+        // max while the block max is reduced alongside; only a max that grew by more than
+        // 2^8 (rare) sends the block through a second pass.  A row's first visible keys
+        // (m = -inf) take the second pass too: their max is not known in advance.
+        const float mref = m == -INFINITY ? 0.f : m;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) t[k] = ((vis >> k) & 1ull) ? t[k] * c : -INFINITY;
-        const float bm = max64(t);
-        float alpha = 1.f;
-        if (bm > m + kRescaleThreshold) {  // also true for the first visible keys (m = -inf)
-          if (l > 0.f) alpha = ex2(m - bm);
-          m = bm;
-        }
-        const float mm = m == -INFINITY ? 0.f : m;  // all keys so far masked: every p is 0
+        for (int k = 0; k < 64; ++k) t[k] = ((vis >> k) & 1ull) ? fmaf(t[k], c, -mref) : -INFINITY;
         uint32_t pk[32];
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 64; k += 2) {
-          const float p0 = ex2(t[k] - mm), p1 = ex2(t[k + 1] - mm);
+          const float p0 = ex2(t[k]), p1 = ex2(t[k + 1]);
           s4[(k >> 1) & 3] += p0 + p1;
           pk[k >> 1] = pack_bf16(p0, p1);
+        }
+        const float bmt = max64(t);  // block max relative to mref
+        float alpha = 1.f;
+        if (bmt > (m == -INFINITY ? -INFINITY : kRescaleThreshold)) {
+          if (l > 0.f) alpha = ex2(-bmt);
+          m = mref + bmt;
+          s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            const float p0 = ex2(t[k] - bmt), p1 = ex2(t[k + 1] - bmt);
+            s4[(k >> 1) & 3] += p0 + p1;
+            pk[k >> 1] = pack_bf16(p0, p1);
+          }
         }
         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         l = l * alpha + sum;
@@ -496,8 +507,10 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
       uint32_t u = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
+        int next_row = it.nb > 0 ? (int)block_row0(p, it, sweep_block(it, 0)) : 0;
         for (int j = 0; j < it.nb; ++j) {
-          const int row0 = (int)block_row0(p, it, sweep_block(it, j));
+          const int row0 = next_row;
+          if (j + 1 < it.nb) next_row = (int)block_row0(p, it, sweep_block(it, j + 1));
           for (int h = 0; h < 2; ++h, ++u) {
             const uint32_t st = u % kNLS;
             // rank 0 has read the stage's previous fill and re-armed its barrier
@@ -515,8 +528,10 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
       uint32_t u = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
+        int next_row = it.nb > 0 ? (int)block_row0(p, it, sweep_block(it, 0)) : 0;
         for (int j = 0; j < it.nb; ++j) {
-          const int row0 = (int)block_row0(p, it, sweep_block(it, j));
+          const int row0 = next_row;
+          if (j + 1 < it.nb) next_row = (int)block_row0(p, it, sweep_block(it, j + 1));
           for (int h = 0; h < 2; ++h, ++u) {
             const uint32_t st = u % kNLO;
             if (!wait_bar(sh, &sh.olat_consumed[st], ((u / kNLO) & 1) ^ 1, p.status)) return;

@@ -13,25 +13,28 @@
 // tensor memory, leaving no room for S.  So each tile is served by a cluster of two CTAs
 // on two SMs that split the two contractions between them:
 //
-//   rank 0 ("S side"): holds the tile's queries in TMEM (A operand of QK^T), receives each
-//     64-key block's latent rows (two 3-D boxes of 4 chunks, loaded for it by rank 1's TMA
-//     engine) and loads the rope chunk itself, computes S into one of two TMEM
-//     buffers, runs the masked online softmax (lazy rescaling: the running max only moves
-//     when it grows by more than 2^8), and ships each block's P (bf16, in the swizzled
-//     K-major layout the MMA reads), the per-row rescale factors and, at the end, the row
-//     sums to rank 1 with one bulk shared->shared copy per block.  It writes the lse.
-//   rank 1 ("O side"): streams the same keys' latent chunks as the V operand (MN-major
-//     B), accumulates O += P V in all 512 TMEM columns, applies the rare rescales, and at
-//     the end of the tile normalises O by the row sums and writes it out.
+//   rank 0 ("S side"): holds the tile's latent queries in TMEM (A operand of QK^T) and
+//     their rope part in shared memory, loads the keys 128 at a time (two 3-D boxes of
+//     4 latent chunks and one rope box), computes S for 128 keys into one of two TMEM
+//     buffers with N = 128 MMAs, runs the masked online softmax (lazy rescaling: the
+//     running max only moves when a block's max exceeds it by more than 2^8), and stores
+//     each 64-key half's P (bf16, in the swizzled K-major layout the MMA reads), the per-row
+//     rescale factor and running row sum straight into rank 1's shared memory with
+//     st.async, whose byte count completes rank 1's inbox barrier.  It writes the lse.
+//   rank 1 ("O side"): streams each 64-key block's latent chunks as the V operand
+//     (MN-major B), accumulates O += P V in all 512 TMEM columns, applies the rare
+//     rescales, and at the end of the tile normalises O by the row sums and writes it out.
 //
-// Per 64-key block the S side does 2*128*64*576 flops and the O side 2*128*512*64, so
-// the pair is balanced to within 12%.  Warp roles per CTA (256 threads): warp 0 = TMA
-// producer, warp 1 = MMA issuer (and TMEM allocator), warp 2 = message sender on rank 0
-// and message bookkeeping on rank 1, warps 4-7 = the row-parallel math (thread = tile
-// row, matching TMEM lanes).  Messages travel through 2 staging buffers on rank 0 and 4
-// inbox buffers on rank 1, so the softmax never waits for the peer's round trip.
-// Tiles are handed out round-robin to the persistent clusters; long KV ranges may be
-// split across tiles and merged by the split combine kernel.
+// Per 128 keys the S side issues 36 MMAs of 128x128x16 and the O side 16 of 128x256x16,
+// so the pair is balanced to within 12%.  Warp roles per CTA (256 threads): warp 0 = TMA
+// producer, warp 1 = MMA issuer (and TMEM allocator), warps 4-7 = the row-parallel math
+// (thread = tile row, matching TMEM lanes); warps 2-3 idle.
+//
+// Keys come from a row-major view of the cache (c_kv row, k_pe row per key).  A 128-key
+// box needs 128 consecutive rows, so a paged cache (64-key pages in any order) is first
+// gathered into a contiguous copy in the workspace by gather_kv_kernel; a contiguous
+// cache is read in place.  Tiles are handed out round-robin to the persistent clusters;
+// long KV ranges may be split across tiles and merged by the split combine kernel.
 //
 // Every wait is bounded (a wall-clock deadline); on expiry the kernel records
 // TV_ERR_TIMEOUT, tells the peer CTA, drains its tensor-core work, frees its TMEM and
@@ -52,39 +55,41 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kDL = 512, kDR = 64, kBN = 64, kRows = 128;
-constexpr int kChunkBytes = kBN * 128;          // 64 keys x 64 bf16
-constexpr int kKChunks = 9;                     // 8 latent + 1 rope chunk per key block
-constexpr int kHalf = 4 * kChunkBytes;          // 4 latent chunks: one 3-D TMA box
-constexpr int kNLS = 5;                         // S-side latent ring stages (half key blocks)
+constexpr int kDL = 512, kDR = 64, kBN = 64, kStep = 128, kRows = 128;
+constexpr int kChunkS = kStep * 128;            // 128 keys x 64 bf16 (S side)
+constexpr int kStageS = 4 * kChunkS;            // 4 latent chunks: one 3-D box
+constexpr int kNLS = 3;                         // S-side latent ring stages
+constexpr int kChunkO = kBN * 128;              // 64 keys x 64 bf16 (O side)
+constexpr int kHalfO = 4 * kChunkO;             // 4 latent chunks of a 64-key block
 constexpr int kNLO = 4;                         // O-side latent ring stages
-constexpr int kNR = 2;                          // S-side rope ring stages
-constexpr int kMsgAlpha = 16384, kMsgL = 16896, kMsgHdr = 17408, kMsgBytes = 17424;
+// A message carries one 64-key block: P (128 rows x 64 keys bf16), then per row the
+// rescale factor and running row sum (fp32), then one flags word.
+constexpr int kMsgAlpha = 16384, kMsgL = 16896, kMsgFlags = 17408;
+constexpr uint32_t kMsgBytes = 17412;
 constexpr int kMsgStride = 18432;
-constexpr int kNStage = 2;                      // S-side staging buffers
-constexpr int kNInbox = 4;                      // O-side inbox buffers
+constexpr int kNInbox = 4;
 constexpr int kThreads = 256;
-// Shared memory, from offset 0 in each CTA: its own latent ring (both are filled by rank
-// 1's TMA engine: rank 0's through a multicast addressed to rank 0 only), then on rank 0
-// the rope ring and the staging buffers, on rank 1 the inbox.
-constexpr int kLatS = kNLS * kHalf;
-constexpr int kLatO = kNLO * kHalf;
-constexpr int kSideA = kLatS + kNR * kChunkBytes + kNStage * kMsgStride;
-constexpr int kSideB = kLatO + kNInbox * kMsgStride;
+// Shared memory, from offset 0 in each CTA.  Rank 0: latent ring, rope stage, the tile's
+// rope queries.  Rank 1: latent ring, inbox.
+constexpr int kRopeOff = kNLS * kStageS;
+constexpr int kQropeOff = kRopeOff + kChunkS;
+constexpr int kSideA = kQropeOff + kRows * 128;
+constexpr int kInboxOff = kNLO * kHalfO;
+constexpr int kSideB = kInboxOff + kNInbox * kMsgStride;
 constexpr int kSmemBytes = (kSideA > kSideB ? kSideA : kSideB) + 1024;
-constexpr uint32_t kTmQ = 0, kTmS0 = 288, kTmS1 = 352;       // S-side TMEM columns
-constexpr uint32_t kFlagFirst = 1, kFlagRescale = 2, kFlagFinal = 4;
+constexpr uint32_t kTmQ = 0, kTmS0 = 256, kTmS1 = 384;       // S-side TMEM columns
+constexpr uint32_t kFlagRescale = 2;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, 0, 0);
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
 
 struct TcParams {
   const __nv_bfloat16* q_latent;
   const __nv_bfloat16* q_pe;
-  const int32_t* page_table;
-  int64_t kv_stride_b;
+  int64_t seq_rows;  // rows between consecutive sequences in the key view
+  int64_t seq_cap;   // longest KV a sequence may have
   const int32_t* prefix_len;
   const uint64_t* anc;
   float* out;
@@ -93,20 +98,18 @@ struct TcParams {
   float* ws_lse;
   int32_t* status;
   int64_t rows_total;  // B*Q*H
-  int32_t max_pages;
   int32_t B, H, Q, max_prefix;
   int32_t tiles_per_seq, splits, chunk, n_items;
-  int32_t paged;
   float scale_log2;
 };
 
 struct Shared {
-  uint64_t slat_full[kNLS], slat_consumed[kNLS], slat_empty[kNLS];
-  uint64_t olat_full[kNLO], olat_consumed[kNLO];
-  uint64_t rope_full[kNR], rope_empty[kNR];
+  uint64_t slat_full[kNLS], slat_empty[kNLS];
+  uint64_t olat_full[kNLO], olat_empty[kNLO];
+  uint64_t rope_full, rope_empty;
   uint64_t s_full[2], s_empty[2];
-  uint64_t q_ready, q_free, msg_ready[kNStage], staging_free[kNStage], pdst_free[kNInbox];
-  uint64_t p_full[kNInbox], p_consumed[kNInbox];
+  uint64_t q_ready, q_free, pdst_free[kNInbox];
+  uint64_t p_full[kNInbox];
   uint64_t drain, job_full, corr_done, epi_done, final_bar;
   uint32_t tmem_base;
   volatile int abort;
@@ -115,7 +118,8 @@ struct Shared {
 
 struct Item {
   int b, t, s, P, nb;
-  int rot;  // first key block of this tile's sweep (see decode)
+  int ns;   // 128-key steps: ceil(nb / 2)
+  int rot;  // first step of this tile's sweep (see decode)
   int64_t k0;
   bool bad;
 };
@@ -128,23 +132,28 @@ __device__ __noinline__ Item decode(const TcParams& p, int item) {
   it.b = bs / p.splits;
   it.P = p.prefix_len[it.b];
   const int64_t kv_len = (int64_t)it.P + p.Q;
-  it.bad = it.P < 0 || it.P > p.max_prefix ||
-           (p.paged ? kv_len > (int64_t)p.max_pages * kBN : kv_len > p.kv_stride_b);
+  it.bad = it.P < 0 || it.P > p.max_prefix || kv_len > p.seq_cap;
   it.k0 = (int64_t)it.s * p.chunk;
   int64_t k1 = it.k0 + p.chunk < kv_len ? it.k0 + p.chunk : kv_len;
   if (it.bad) k1 = it.k0;
   it.nb = k1 > it.k0 ? (int)((k1 - it.k0 + kBN - 1) / kBN) : 0;
+  it.ns = (it.nb + 1) >> 1;
   // The row tiles of one sequence run at the same time on neighbouring clusters; each
-  // starts its sweep over the key blocks at a different block so that they do not all
+  // starts its sweep over the key steps at a different step so that they do not all
   // request the same cache lines at once (the softmax is independent of block order).
-  it.rot = it.nb > 0 ? (int)(((int64_t)it.t * it.nb) / p.tiles_per_seq) : 0;
+  it.rot = it.ns > 0 ? (int)(((int64_t)it.t * it.ns) / p.tiles_per_seq) : 0;
   return it;
 }
 
-// Key block visited at step j of the tile's sweep.
-__device__ __forceinline__ int sweep_block(const Item& it, int j) {
+// 128-key step visited at position j of the tile's sweep; it holds the 64-key blocks
+// 2*step and (if it exists) 2*step + 1.
+__device__ __forceinline__ int sweep_step(const Item& it, int j) {
   const int jj = j + it.rot;
-  return jj >= it.nb ? jj - it.nb : jj;
+  return jj >= it.ns ? jj - it.ns : jj;
+}
+
+__device__ __forceinline__ int64_t key_row(const TcParams& p, const Item& it, int64_t key) {
+  return (int64_t)it.b * p.seq_rows + it.k0 + key;
 }
 
 __device__ __forceinline__ void raise_abort(Shared& sh, int32_t* status, int code) {
@@ -181,12 +190,6 @@ __device__ __forceinline__ bool wait_bar(Shared& sh, uint64_t* bar, uint32_t par
   return wait_bar_slow(sh, a, parity, status);
 }
 
-__device__ __forceinline__ int64_t block_row0(const TcParams& p, const Item& it, int j) {
-  const int64_t key0 = it.k0 + (int64_t)j * kBN;
-  if (p.paged) return (int64_t)p.page_table[(int64_t)it.b * p.max_pages + key0 / kBN] * kBN;
-  return (int64_t)it.b * p.kv_stride_b + key0;
-}
-
 // Visibility of keys key0 .. key0+63 for a row whose node has ancestor bitset `anc`: bit k
 // set iff key0 + k < k1 and (key0 + k is a prefix key, or the tree node key0 + k - P is an
 // ancestor-or-self of the row's node).
@@ -200,90 +203,101 @@ __device__ __forceinline__ uint64_t block_vis(int64_t key0, int64_t P, int64_t k
   return (pm | tm) & rm;
 }
 
-__device__ __forceinline__ float max64(const float* t) {
-  float a[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a[i] = fmaxf(fmaxf(t[4 * i], t[4 * i + 1]), fmaxf(t[4 * i + 2], t[4 * i + 3]));
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
-  return a[0];
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One 64-key half of a step: p = 2^(s*c - mr) for the 64 scores (masked ones are -inf),
+// packed to bf16 and stored with st.async into the peer's inbox row; returns the sum.
+__device__ __forceinline__ float emit_half(const float* t, float c, float mr, uint32_t row_dst,
+                                           uint32_t sw, uint32_t bar) {
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float p0 = ex2(fmaf(t[8 * q + 2 * e], c, -mr));
+      const float p1 = ex2(fmaf(t[8 * q + 2 * e + 1], c, -mr));
+      s4[e] += p0 + p1;
+      w[e] = pack_bf16(p0, p1);
+    }
+    st_async_v4(row_dst + (((uint32_t)q ^ sw) << 4), w[0], w[1], w[2], w[3], bar);
+  }
+  return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
 // ===================================================================================
 // rank 0: QK^T + softmax
 // ===================================================================================
-__device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUtensorMap* map_kpe,
+__device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUtensorMap* map_kpe,
                        Shared& sh, unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* lat = smem;
-  unsigned char* rope = smem + kLatS;
-  unsigned char* stage = rope + kNR * kChunkBytes;
+  unsigned char* rope = smem + kRopeOff;
+  unsigned char* qrope = smem + kQropeOff;
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer: the rope chunk of each key block ----------------
-    // (the latent chunks arrive by multicast from rank 1's producer)
+    // ---------------- TMA producer: two latent boxes and the rope box per step ---------
     if (lane == 0) {
+      prefetch_tensormap(map_lat);
       prefetch_tensormap(map_kpe);
-      uint32_t kb = 0;
+      uint32_t u = 0, rc = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
-        // the page-table lookup for the next block is issued a block ahead
-        int next_row = it.nb > 0 ? (int)block_row0(p, it, sweep_block(it, 0)) : 0;
-        for (int j = 0; j < it.nb; ++j, ++kb) {
-          const int row0 = next_row;
-          if (j + 1 < it.nb) next_row = (int)block_row0(p, it, sweep_block(it, j + 1));
-          const uint32_t st = kb % kNR;
-          if (!wait_bar(sh, &sh.rope_empty[st], ((kb / kNR) & 1) ^ 1, p.status)) return;
-          mbar_arrive_expect_tx(&sh.rope_full[st], kChunkBytes);
-          tma_load_2d(rope + st * kChunkBytes, map_kpe, 0, row0, &sh.rope_full[st]);
+        for (int j = 0; j < it.ns; ++j, ++rc) {
+          const int row0 = (int)key_row(p, it, (int64_t)sweep_step(it, j) * kStep);
+          for (int h = 0; h < 2; ++h, ++u) {
+            const uint32_t st = u % kNLS;
+            if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
+            mbar_arrive_expect_tx(&sh.slat_full[st], kStageS);
+            tma_load_3d(lat + st * kStageS, map_lat, 0, row0, 4 * h, &sh.slat_full[st]);
+          }
+          if (!wait_bar(sh, &sh.rope_empty, (rc & 1) ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.rope_full, kChunkS);
+          tma_load_2d(rope, map_kpe, 0, row0, &sh.rope_full);
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: S = Q K^T -----------------------------------------
+    // ---------------- MMA issuer: S = Q K^T, 128 keys per step ----------------------
     if (lane == 0) {
-      uint32_t kb = 0, sc = 0, qc = 0;
+      uint32_t u = 0, sc = 0, qc = 0, rc = 0;
+      const uint32_t qa = smem_u32(qrope), ra = smem_u32(rope);
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
-        if (it.nb == 0) continue;
+        if (it.ns == 0) continue;
         if (!wait_bar(sh, &sh.q_ready, qc & 1, p.status)) break;
         ++qc;
         tc_fence_after();
-        for (int j = 0; j < it.nb && !sh.abort; ++j, ++sc, ++kb) {
+        for (int j = 0; j < it.ns && !sh.abort; ++j, ++sc, ++rc) {
           const uint32_t sb = sc & 1;
           if (!wait_bar(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
           tc_fence_after();  // the softmax warps' TMEM reads of this S buffer come first
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
           bool ok = true;
-          for (int h = 0; h < 2 && ok; ++h) {
-            const uint32_t u = 2 * kb + h, st = u % kNLS;
+          for (int h = 0; h < 2 && ok; ++h, ++u) {
+            const uint32_t st = u % kNLS;
             if (!wait_bar(sh, &sh.slat_full[st], (u / kNLS) & 1, p.status)) { ok = false; break; }
-            const uint32_t sa = smem_u32(lat + st * kHalf);
+            const uint32_t sa = smem_u32(lat + st * kStageS);
+#pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 mma_ts(d, tmem + kTmQ + 32 * (4 * h + c) + 8 * kk,
-                       smem_desc(sa + c * kChunkBytes + 32 * kk, 16, 1024, 2), kIdescQK,
+                       smem_desc(sa + c * kChunkS + 32 * kk, 16, 1024, 2), kIdescQK,
                        (h | c | kk) != 0);
-            mma_commit(&sh.slat_consumed[st]);
+            mma_commit(&sh.slat_empty[st]);
           }
-          const uint32_t rs = kb % kNR;
-          if (!ok || !wait_bar(sh, &sh.rope_full[rs], (kb / kNR) & 1, p.status)) break;
-          const uint32_t ra = smem_u32(rope + rs * kChunkBytes);
+          if (!ok || !wait_bar(sh, &sh.rope_full, rc & 1, p.status)) break;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(d, tmem + kTmQ + 32 * 8 + 8 * kk, smem_desc(ra + 32 * kk, 16, 1024, 2),
+            mma_ss(d, smem_desc(qa + 32 * kk, 16, 1024, 2), smem_desc(ra + 32 * kk, 16, 1024, 2),
                    kIdescQK, 1);
-          mma_commit(&sh.rope_empty[rs]);
+          mma_commit(&sh.rope_empty);
           mma_commit(&sh.s_full[sb]);
         }
         mma_commit(&sh.q_free);
@@ -291,68 +305,23 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
       mma_commit(&sh.final_bar);
       wait_bar(sh, &sh.final_bar, 0, p.status);
     }
-  } else if (warp == 3) {
-    // ---------------- latent-ring helper: once this CTA has read a stage, re-arm it and
-    // tell rank 1's producer for this ring that the stage may be refilled ---------------
-    if (lane == 0) {
-      const uint32_t peer = cluster_rank() ^ 1u;
-      uint32_t u = 0;
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
-        const Item it = decode(p, item);
-        for (int j = 0; j < 2 * it.nb; ++j, ++u) {
-          const uint32_t st = u % kNLS;
-          if (!wait_bar(sh, &sh.slat_consumed[st], (u / kNLS) & 1, p.status)) return;
-          mbar_arrive_expect_tx(&sh.slat_full[st], kHalf);
-          mbar_arrive_remote(map_to_rank(smem_u32(&sh.slat_empty[st]), peer));
-        }
-      }
-    }
-  } else if (warp == 2) {
-    // ---------------- sender: staging buffer -> peer inbox, one bulk copy per block --
-    const uint32_t peer = cluster_rank() ^ 1u;
-    unsigned char* peer_inbox_local = smem + kLatO;  // same offset in the peer
-    uint32_t mc = 0;
-    bool live = true;
-    for (int item = cid; item < p.n_items && live && !sh.abort; item += ncl) {
-      const Item it = decode(p, item);
-      for (int j = 0; j < it.nb; ++j, ++mc) {
-        const uint32_t sbuf = mc % kNStage, ib = mc % kNInbox;
-        if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.msg_ready[sbuf], (mc / kNStage) & 1, p.status))) {
-          live = false;
-          break;
-        }
-        unsigned char* msg = stage + sbuf * kMsgStride;
-        const float* alpha = reinterpret_cast<const float*>(msg + kMsgAlpha);
-        bool resc = false;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) resc |= alpha[lane * 4 + q] != 1.f;
-        resc = __any_sync(0xffffffffu, resc);
-        if (lane == 0) {
-          const uint32_t flags = (j == 0 ? kFlagFirst : 0u) | (j == it.nb - 1 ? kFlagFinal : 0u) |
-                                 ((resc && j > 0) ? kFlagRescale : 0u);
-          *reinterpret_cast<volatile uint32_t*>(msg + kMsgHdr) = flags;
-          fence_proxy_async_smem();
-          if (wait_bar(sh, &sh.pdst_free[ib], ((mc / kNInbox) & 1) ^ 1, p.status)) {
-            const uint32_t dst = map_to_rank(smem_u32(peer_inbox_local + ib * kMsgStride), peer);
-            const uint32_t bar = map_to_rank(smem_u32(&sh.p_full[ib]), peer);
-            bulk_copy_to_cluster(dst, msg, kMsgBytes, bar);
-            bulk_commit();
-            bulk_wait_read<0>();
-          }
-          mbar_arrive(&sh.staging_free[sbuf]);
-        }
-        __syncwarp();
-      }
-    }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   } else if (warp >= 4) {
     // ---------------- softmax warpgroup: thread r owns tile row r ------------------
     const int wq = warp - 4;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float c = p.scale_log2;
+    const uint32_t peer = cluster_rank() ^ 1u;
+    // this row's place in every inbox buffer of the peer, and the buffers' barriers
+    const uint32_t inbox_peer = map_to_rank(smem_u32(smem + kInboxOff), peer);
+    const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+    const uint32_t sw = (uint32_t)(r & 7);
+    // The four warps leave their loops only together, at a 128-thread barrier that agrees
+    // on the outcome of the waits before it (a warp that left alone would strand the
+    // others at the next barrier).
     uint32_t sc = 0, qc = 0, mc = 0;
-    for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+    bool live = true;
+    for (int item = cid; item < p.n_items && live; item += ncl) {
       const Item it = decode(p, item);
       const int trow = it.t * kRows + r;
       const bool vrow = trow < p.Q * p.H;
@@ -382,24 +351,25 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
       const int64_t kv_end = (int64_t)it.P + p.Q;
       const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
 
-      // ---- queries of this row into TMEM columns [0, 288) ----
-      // (each warp agrees on the outcome of a wait before its warp-collective TMEM ops)
-      if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) break;
+      // ---- latent queries into TMEM columns [0, 256), rope queries into shared memory ----
+      if (!named_sync_and(3, 128, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) {
+        live = false;
+        break;
+      }
       ++qc;
       tc_fence_after();
       {
         const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + grow * kDL);
         const uint4* qr = reinterpret_cast<const uint4*>(p.q_pe + grow * kDR);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kKChunks; c0 += 3) {
-          uint32_t w[3][32];
+        for (int c0 = 0; c0 < 8; c0 += 2) {
+          uint32_t w[2][32];
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc) {
-            const int ch = c0 + cc;
+          for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               uint4 v = make_uint4(0, 0, 0, 0);
-              if (vrow) v = ch < 8 ? __ldg(ql + 8 * ch + e) : __ldg(qr + e);
+              if (vrow) v = __ldg(ql + 8 * (c0 + cc) + e);
               w[cc][4 * e + 0] = v.x;
               w[cc][4 * e + 1] = v.y;
               w[cc][4 * e + 2] = v.z;
@@ -408,80 +378,114 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
           }
           __syncwarp();
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc) tmem_st32(tmem + lane_base + kTmQ + 32 * (c0 + cc), w[cc]);
+          for (int cc = 0; cc < 2; ++cc) tmem_st32(tmem + lane_base + kTmQ + 32 * (c0 + cc), w[cc]);
+        }
+        unsigned char* qrow = qrope + row_off;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (vrow) v = __ldg(qr + e);
+          *reinterpret_cast<uint4*>(qrow + (((uint32_t)e ^ sw) << 4)) = v;
         }
       }
       tmem_wait_st();
+      fence_proxy_async_smem();  // the rope queries are read by the MMAs
       tc_fence_before();
       mbar_arrive(&sh.q_ready);
 
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < it.nb; ++j, ++sc, ++mc) {
+      for (int j = 0; j < it.ns; ++j, ++sc) {
         const uint32_t sb = sc & 1;
-        if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.s_full[sb], (sc >> 1) & 1, p.status))) break;
-        tc_fence_after();
-        float t[64];
-        {
-          uint32_t sr[64];
-          tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0), sr);
-          tmem_ld32(tmem + lane_base + (sb ? kTmS1 : kTmS0) + 32, sr + 32);
+        // each warp agrees before its warp-collective TMEM loads
+        const bool okf =
+            __all_sync(0xffffffffu, wait_bar(sh, &sh.s_full[sb], (sc >> 1) & 1, p.status));
+        float t[128];
+        if (!okf) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k) t[k] = 0.f;
+        } else {
+          tc_fence_after();
+          uint32_t sr[128];
+          const uint32_t ta = tmem + lane_base + (sb ? kTmS1 : kTmS0);
+          tmem_ld32(ta, sr);
+          tmem_ld32(ta + 32, sr + 32);
+          tmem_ld32(ta + 64, sr + 64);
+          tmem_ld32(ta + 96, sr + 96);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(&sh.s_empty[sb]);
 #pragma unroll
-          for (int k = 0; k < 64; ++k) t[k] = __uint_as_float(sr[k]);
+          for (int k = 0; k < 128; ++k) t[k] = __uint_as_float(sr[k]);
         }
-        const int64_t key0 = it.k0 + (int64_t)sweep_block(it, j) * kBN;
-        const uint64_t vis =
+        const int st = sweep_step(it, j);
+        const bool two = 2 * st + 1 < it.nb;
+        const int64_t key0 = it.k0 + (int64_t)st * kStep;
+        const uint64_t vis0 =
             (key0 + kBN > it.P || key0 + kBN > k1) ? block_vis(key0, it.P, k1, anc) : ~0ull;
-
-        // t = score*c - m (masked keys -inf), exponentiated against the current running
-        // max while the block max is reduced alongside; only a max that grew by more than
-        // 2^8 (rare) sends the block through a second pass.  A row's first visible keys
-        // (m = -inf) take the second pass too: their max is not known in advance.
-        const float mref = m == -INFINITY ? 0.f : m;
+        const uint64_t vis1 =
+            !two ? 0ull
+                 : ((key0 + 2 * kBN > it.P || key0 + 2 * kBN > k1)
+                        ? block_vis(key0 + kBN, it.P, k1, anc)
+                        : ~0ull);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) t[k] = ((vis >> k) & 1ull) ? fmaf(t[k], c, -mref) : -INFINITY;
-        uint32_t pk[32];
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < 64; ++k) t[k] = ((vis0 >> k) & 1ull) ? t[k] : -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const float p0 = ex2(t[k]), p1 = ex2(t[k + 1]);
-          s4[(k >> 1) & 3] += p0 + p1;
-          pk[k >> 1] = pack_bf16(p0, p1);
+        for (int k = 0; k < 64; ++k) t[64 + k] = ((vis1 >> k) & 1ull) ? t[64 + k] : -INFINITY;
+        float mx;
+        {
+          float a[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            a[i] = fmaxf(fmaxf(fmaxf(t[8 * i], t[8 * i + 1]), fmaxf(t[8 * i + 2], t[8 * i + 3])),
+                         fmaxf(fmaxf(t[8 * i + 4], t[8 * i + 5]), fmaxf(t[8 * i + 6], t[8 * i + 7])));
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
+          mx = a[0] * c;  // block max of score*scale in log2 units (-inf if all masked)
         }
-        const float bmt = max64(t);  // block max relative to mref
+        // The running max m moves only when the block max exceeds it by more than 2^8;
+        // then O and l are rescaled by alpha = 2^(m_old - m_new).
         float alpha = 1.f;
-        if (bmt > (m == -INFINITY ? -INFINITY : kRescaleThreshold)) {
-          if (l > 0.f) alpha = ex2(-bmt);
-          m = mref + bmt;
-          s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
-#pragma unroll
-          for (int k = 0; k < 64; k += 2) {
-            const float p0 = ex2(t[k] - bmt), p1 = ex2(t[k + 1] - bmt);
-            s4[(k >> 1) & 3] += p0 + p1;
-            pk[k >> 1] = pack_bf16(p0, p1);
-          }
+        if (mx > (m == -INFINITY ? -INFINITY : m + kRescaleThreshold)) {
+          if (l > 0.f) alpha = ex2(m - mx);
+          m = mx;
         }
-        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        l = l * alpha + sum;
+        const float mr = m == -INFINITY ? 0.f : m;
 
-        // ---- P (bf16, swizzled K-major), alpha and, last, the row sum into staging ----
-        const uint32_t sbuf = mc % kNStage;
-        if (!__all_sync(0xffffffffu,
-                        wait_bar(sh, &sh.staging_free[sbuf], ((mc / kNStage) & 1) ^ 1, p.status)))
+        // ---- wait until the peer's inbox buffers for this step's messages are free ----
+        const uint32_t ib0 = mc % kNInbox, ib1 = (mc + 1) % kNInbox;
+        bool okw = okf && wait_bar(sh, &sh.pdst_free[ib0], ((mc / kNInbox) & 1) ^ 1, p.status);
+        if (two && okw)
+          okw = wait_bar(sh, &sh.pdst_free[ib1], (((mc + 1) / kNInbox) & 1) ^ 1, p.status);
+        // one barrier for the four warps: agree on the outcome and OR the rescale flag
+        const bool resc = named_sync_or(1, 128, alpha != 1.f);
+        if (!named_sync_and(2, 128, okw)) {
+          live = false;
           break;
-        unsigned char* msg = stage + sbuf * kMsgStride;
-        unsigned char* rowp = msg + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(rowp + ((q ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        reinterpret_cast<float*>(msg + kMsgAlpha)[r] = alpha;
-        if (j == it.nb - 1) reinterpret_cast<float*>(msg + kMsgL)[r] = l;
-        fence_proxy_async_smem();
-        mbar_arrive(&sh.msg_ready[sbuf]);
+        }
+
+        const uint32_t dst0 = inbox_peer + ib0 * kMsgStride;
+        const uint32_t bar0 = map_to_rank(smem_u32(&sh.p_full[ib0]), peer);
+        float sum = emit_half(t, c, mr, dst0 + row_off, sw, bar0);
+        uint32_t dst1 = 0, bar1 = 0;
+        if (two) {
+          dst1 = inbox_peer + ib1 * kMsgStride;
+          bar1 = map_to_rank(smem_u32(&sh.p_full[ib1]), peer);
+          sum += emit_half(t + 64, c, mr, dst1 + row_off, sw, bar1);
+        }
+        l = l * alpha + sum;
+        st_async_b32(dst0 + kMsgAlpha + 4 * r, __float_as_uint(alpha), bar0);
+        st_async_b32(dst0 + kMsgL + 4 * r, __float_as_uint(l), bar0);
+        if (r == 0) st_async_b32(dst0 + kMsgFlags, resc ? kFlagRescale : 0u, bar0);
+        if (two) {
+          st_async_b32(dst1 + kMsgAlpha + 4 * r, __float_as_uint(1.f), bar1);
+          st_async_b32(dst1 + kMsgL + 4 * r, __float_as_uint(l), bar1);
+          if (r == 0) st_async_b32(dst1 + kMsgFlags, 0u, bar1);
+        }
+        mc += two ? 2 : 1;
       }
+      if (!live) break;
       if (vrow && !sh.abort)
         *lse_dst = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
@@ -491,52 +495,32 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_ckv, const CUte
 // ===================================================================================
 // rank 1: O += P V, rescale, epilogue
 // ===================================================================================
-__device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh,
+__device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh,
                        unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* lat = smem;
-  unsigned char* inbox = smem + kLatO;
+  unsigned char* inbox = smem + kInboxOff;
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer for rank 0's latent ring (multicast addressed to rank
-    // 0 only, so this CTA's engine serves both rings) ----------------------------------
+    // ---------------- TMA producer: each 64-key block's latent chunks, in message order --
     if (lane == 0) {
-      prefetch_tensormap(map_ckv);
+      prefetch_tensormap(map_lat);
       uint32_t u = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
-        int next_row = it.nb > 0 ? (int)block_row0(p, it, sweep_block(it, 0)) : 0;
-        for (int j = 0; j < it.nb; ++j) {
-          const int row0 = next_row;
-          if (j + 1 < it.nb) next_row = (int)block_row0(p, it, sweep_block(it, j + 1));
-          for (int h = 0; h < 2; ++h, ++u) {
-            const uint32_t st = u % kNLS;
-            // rank 0 has read the stage's previous fill and re-armed its barrier
-            if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
-            tma_load_3d_multicast(lat + st * kHalf, map_ckv, 0, row0, 4 * h, &sh.slat_full[st],
-                                  (uint16_t)0x1);
-          }
-        }
-      }
-    }
-  } else if (warp == 3) {
-    // ---------------- TMA producer for this CTA's latent ring ---------------------------
-    if (lane == 0) {
-      prefetch_tensormap(map_ckv);
-      uint32_t u = 0;
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
-        const Item it = decode(p, item);
-        int next_row = it.nb > 0 ? (int)block_row0(p, it, sweep_block(it, 0)) : 0;
-        for (int j = 0; j < it.nb; ++j) {
-          const int row0 = next_row;
-          if (j + 1 < it.nb) next_row = (int)block_row0(p, it, sweep_block(it, j + 1));
-          for (int h = 0; h < 2; ++h, ++u) {
-            const uint32_t st = u % kNLO;
-            if (!wait_bar(sh, &sh.olat_consumed[st], ((u / kNLO) & 1) ^ 1, p.status)) return;
-            mbar_arrive_expect_tx(&sh.olat_full[st], kHalf);
-            tma_load_3d(lat + st * kHalf, map_ckv, 0, row0, 4 * h, &sh.olat_full[st]);
+        for (int j = 0; j < it.ns; ++j) {
+          const int st = sweep_step(it, j);
+          const int nh = 2 * st + 1 < it.nb ? 2 : 1;
+          for (int hh = 0; hh < nh; ++hh) {
+            const int row0 = (int)key_row(p, it, (int64_t)(2 * st + hh) * kBN);
+            for (int h = 0; h < 2; ++h, ++u) {
+              const uint32_t ls = u % kNLO;
+              if (!wait_bar(sh, &sh.olat_empty[ls], ((u / kNLO) & 1) ^ 1, p.status)) return;
+              mbar_arrive_expect_tx(&sh.olat_full[ls], kHalfO);
+              tma_load_3d(lat + ls * kHalfO, map_lat, 0, row0, 4 * h, &sh.olat_full[ls]);
+            }
           }
         }
       }
@@ -544,21 +528,31 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
   } else if (warp == 1) {
     // ---------------- MMA issuer: O += P V ------------------------------------------
     if (lane == 0) {
-      uint32_t vc = 0, mc = 0, ic = 0, dc = 0, cc = 0;
+      const uint32_t peer = cluster_rank() ^ 1u;
+      uint32_t vc = 0, mc = 0, ic = 0, dc = 0, cc = 0, last_pb = 0;
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
         if (it.nb == 0) continue;
-        if (ic > 0 && !wait_bar(sh, &sh.epi_done, (ic - 1) & 1, p.status)) break;
+        if (ic > 0) {
+          // the previous tile's epilogue has read its last message: hand that buffer back
+          if (!wait_bar(sh, &sh.epi_done, (ic - 1) & 1, p.status)) break;
+          mbar_arrive_remote(map_to_rank(smem_u32(&sh.pdst_free[last_pb]), peer));
+        }
         tc_fence_after();
-        uint32_t last_pb = 0;
         bool ok = true;
         for (int j = 0; j < it.nb && ok; ++j, ++mc) {
           const uint32_t pb = mc % kNInbox;
           last_pb = pb;
           if (!wait_bar(sh, &sh.p_full[pb], (mc / kNInbox) & 1, p.status)) { ok = false; break; }
+          // arm the buffer's next phase now: its next message is only sent after the MMAs
+          // below have read this one
+          mbar_arrive_expect_tx(&sh.p_full[pb], kMsgBytes);
+          // the message arrived through generic-proxy stores; the MMAs read it through the
+          // async proxy
+          fence_proxy_async_smem();
           const uint32_t flags =
-              *reinterpret_cast<volatile uint32_t*>(inbox + pb * kMsgStride + kMsgHdr);
-          if (flags & kFlagRescale) {
+              *reinterpret_cast<volatile uint32_t*>(inbox + pb * kMsgStride + kMsgFlags);
+          if (j > 0 && (flags & kFlagRescale)) {
             mma_commit(&sh.drain);
             if (!wait_bar(sh, &sh.drain, dc & 1, p.status)) { ok = false; break; }
             ++dc;
@@ -573,14 +567,16 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
           for (int h = 0; h < 2; ++h, ++vc) {
             const uint32_t st = vc % kNLO;
             if (!wait_bar(sh, &sh.olat_full[st], (vc / kNLO) & 1, p.status)) { ok = false; break; }
-            const uint32_t va = smem_u32(lat + st * kHalf);
+            const uint32_t va = smem_u32(lat + st * kHalfO);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(tmem + 256 * h, smem_desc(pa + 32 * kk, 16, 1024, 2),
                      smem_desc(va + 2048 * kk, 8192, 1024, 2), kIdescPV, (j | kk) != 0);
-            mma_commit(&sh.olat_consumed[st]);
+            mma_commit(&sh.olat_empty[st]);
           }
-          mma_commit(&sh.p_consumed[pb]);
+          // once the MMAs have read the message, the buffer goes straight back to rank 0's
+          // softmax; a tile's last message stays until the epilogue has read its row sums
+          if (j < it.nb - 1) mma_commit_multicast(&sh.pdst_free[pb], (uint16_t)(1u << peer));
         }
         if (!ok) break;
         mma_commit(&sh.drain);
@@ -596,24 +592,6 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
       mbar_arrive(&sh.job_full);
       mma_commit(&sh.final_bar);
       wait_bar(sh, &sh.final_bar, 0, p.status);
-    }
-  } else if (warp == 2) {
-    // ---------------- inbox bookkeeping: re-arm and hand buffers back ---------------
-    if (lane == 0) {
-      const uint32_t peer = cluster_rank() ^ 1u;
-      uint32_t mc = 0, ic = 0;
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
-        const Item it = decode(p, item);
-        if (it.nb == 0) continue;
-        for (int j = 0; j < it.nb; ++j, ++mc) {
-          const uint32_t pb = mc % kNInbox;
-          if (!wait_bar(sh, &sh.p_consumed[pb], (mc / kNInbox) & 1, p.status)) return;
-          if (j == it.nb - 1 && !wait_bar(sh, &sh.epi_done, ic & 1, p.status)) return;
-          mbar_arrive_expect_tx(&sh.p_full[pb], kMsgBytes);
-          mbar_arrive_remote(map_to_rank(smem_u32(&sh.pdst_free[pb]), peer));
-        }
-        ++ic;
-      }
     }
   } else if (warp >= 4) {
     // ---------------- rescale / epilogue warpgroup: thread r owns tile row r -------
@@ -687,8 +665,9 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_ckv, Shared& sh
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
-               const __grid_constant__ CUtensorMap map_kpe) {
+attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
+               const __grid_constant__ CUtensorMap map_kpe_s,
+               const __grid_constant__ CUtensorMap map_lat_o) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ Shared sh;
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -699,29 +678,21 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNLS; ++i) {
       mbar_init(&sh.slat_full[i], 1);
-      mbar_init(&sh.slat_consumed[i], 1);
       mbar_init(&sh.slat_empty[i], 1);
     }
     for (int i = 0; i < kNLO; ++i) {
       mbar_init(&sh.olat_full[i], 1);
-      mbar_init(&sh.olat_consumed[i], 1);
+      mbar_init(&sh.olat_empty[i], 1);
     }
-    for (int i = 0; i < kNR; ++i) {
-      mbar_init(&sh.rope_full[i], 1);
-      mbar_init(&sh.rope_empty[i], 1);
-    }
+    mbar_init(&sh.rope_full, 1);
+    mbar_init(&sh.rope_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 128);
     }
-    for (int i = 0; i < kNStage; ++i) {
-      mbar_init(&sh.msg_ready[i], 128);
-      mbar_init(&sh.staging_free[i], 1);
-    }
     for (int i = 0; i < kNInbox; ++i) {
       mbar_init(&sh.pdst_free[i], 1);
       mbar_init(&sh.p_full[i], 1);
-      mbar_init(&sh.p_consumed[i], 1);
     }
     mbar_init(&sh.q_ready, 128);
     mbar_init(&sh.q_free, 1);
@@ -733,10 +704,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
     sh.abort = 0;
     sh.job_type = 0;
     sh.job_buf = 0;
-    if (rank == 0) {
-      // rank 0's latent stages start armed for their first fill (issued by rank 1)
-      for (int i = 0; i < kNLS; ++i) mbar_arrive_expect_tx(&sh.slat_full[i], kHalf);
-    }
     if (rank == 1) {
       // every inbox buffer starts armed for its first message
       for (int i = 0; i < kNInbox; ++i) mbar_arrive_expect_tx(&sh.p_full[i], kMsgBytes);
@@ -750,18 +717,49 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_ckv,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // barriers of both CTAs exist before any remote arrive or copy
+  cluster_sync();  // barriers of both CTAs exist before any remote arrive or store
 
   if (rank == 0)
-    s_side(p, &map_ckv, &map_kpe, sh, smem);
+    s_side(p, &map_lat_s, &map_kpe_s, sh, smem);
   else
-    o_side(p, &map_ckv, sh, smem);
+    o_side(p, &map_lat_o, sh, smem);
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(sh.tmem_base, 512);
   cluster_sync();  // neither CTA leaves while the other may still touch its memory
+}
+
+// Copies every in-range 64-key page of a paged cache into a contiguous key view: row
+// b * seq_rows + key holds c_kv (512 bf16) then k_pe (64 bf16) of that key.  One CTA per
+// (page slot, sequence).  A page index that points outside the cache rows is reported as
+// TV_ERR_BOUNDS and its rows are left unwritten (the sequence's result is then undefined,
+// as for any out-of-range input).
+__global__ void __launch_bounds__(256)
+gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint4* __restrict__ kpe,
+                 int64_t kpe_stride16, const int32_t* __restrict__ page_table, int max_pages,
+                 const int32_t* __restrict__ prefix_len, int Q, int max_prefix, int64_t num_rows,
+                 int64_t seq_rows, uint4* __restrict__ out, int32_t* status) {
+  constexpr int kW = (kDL + kDR) * 2 / 16;  // 72 16-byte words per key row
+  const int b = blockIdx.y, j = blockIdx.x;
+  const int P = prefix_len[b];
+  if (P < 0 || P > max_prefix) return;  // reported by the attention kernel
+  const int64_t kv_len = (int64_t)P + Q;
+  if ((int64_t)j * kBN >= kv_len || j >= max_pages) return;
+  const int64_t pg = page_table[(int64_t)b * max_pages + j];
+  if (pg < 0 || (pg + 1) * kBN > num_rows) {
+    if (threadIdx.x == 0) report(status, TV_ERR_BOUNDS);
+    return;
+  }
+  const int64_t src0 = pg * kBN, dst0 = (int64_t)b * seq_rows + (int64_t)j * kBN;
+#pragma unroll 2
+  for (int idx = threadIdx.x; idx < kBN * kW; idx += 256) {
+    const int i = idx / kW, w = idx - i * kW;
+    const uint4 v = w < 64 ? __ldg(ckv + (src0 + i) * ckv_stride16 + w)
+                           : __ldg(kpe + (src0 + i) * kpe_stride16 + (w - 64));
+    out[(dst0 + i) * kW + w] = v;
+  }
 }
 
 // ---- host side -----------------------------------------------------------------------
@@ -783,11 +781,12 @@ bool get_encode() {
 }
 
 // Latent rows viewed as [64 elements][rows][8 chunks of 64 elements]: one box is 4 chunks
-// of 64 rows, landing chunk-major in shared memory as four 128-byte-swizzled 8 KB tiles.
-bool make_map_latent(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes) {
+// of `box_rows` rows, landing chunk-major in shared memory as four 128-byte-swizzled tiles.
+bool make_map_latent(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes,
+                     uint32_t box_rows) {
   cuuint64_t dims[3] = {64, rows, kDL / 64};
   cuuint64_t strides[2] = {row_bytes, 128};
-  cuuint32_t box[3] = {64, 64, 4};
+  cuuint32_t box[3] = {64, box_rows, 4};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -795,11 +794,12 @@ bool make_map_latent(CUtensorMap* m, const void* base, uint64_t rows, uint64_t r
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
-              uint64_t row_bytes) {
-  cuuint64_t dims[2] = {inner, rows};
+// Rope rows: one box is 64 elements of `box_rows` rows.
+bool make_map_rope(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes,
+                   uint32_t box_rows) {
+  cuuint64_t dims[2] = {kDR, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -813,8 +813,10 @@ int max_clusters() {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_max_clusters[dev] == 0) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+                             kSmemBytes) != cudaSuccess) {
+      cudaGetLastError();
       return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 256);
     cfg.blockDim = dim3(kThreads);
@@ -837,12 +839,23 @@ int max_clusters() {
   return g_max_clusters[dev];
 }
 
+// Rows per sequence of the gathered key view: the longest KV rounded up to whole steps.
+int64_t gathered_seq_rows(const tv_attn_args* a) {
+  const int64_t kv_max = (int64_t)a->max_prefix_len + a->Q;
+  return (kv_max + kStep - 1) / kStep * kStep;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
 }  // namespace
 
 bool tc_supported(const tv_attn_args* a) {
-  return a->q_dt == TV_BF16 && a->kv_dt == TV_BF16 && a->d_latent == kDL && a->d_rope == kDR &&
-         a->cache.num_rows > 0 && a->cache.num_rows < (1ll << 31) &&
-         (a->cache.page_table == nullptr || a->cache.page_size == kBN);
+  if (!(a->q_dt == TV_BF16 && a->kv_dt == TV_BF16 && a->d_latent == kDL && a->d_rope == kDR &&
+        a->cache.num_rows > 0 && a->cache.num_rows < (1ll << 31)))
+    return false;
+  if (a->cache.page_table == nullptr) return true;
+  // the gathered copy is addressed with 32-bit TMA row coordinates too
+  return a->cache.page_size == kBN && (int64_t)a->B * gathered_seq_rows(a) < (1ll << 31);
 }
 
 TcPlan tc_plan(const tv_attn_args* a) {
@@ -861,9 +874,10 @@ TcPlan tc_plan(const tv_attn_args* a) {
       splits = (int)std::max<int64_t>(1, std::min(want, cap));
     }
   }
+  // split boundaries fall on whole 128-key steps
   int64_t chunk = (kv_max + splits - 1) / splits;
-  chunk = (chunk + kBN - 1) / kBN * kBN;
-  if (chunk < kBN) chunk = kBN;
+  chunk = (chunk + kStep - 1) / kStep * kStep;
+  if (chunk < kStep) chunk = kStep;
   p.chunk = (int)chunk;
   p.splits = (int)((kv_max + chunk - 1) / chunk);
   if (p.splits < 1) p.splits = 1;
@@ -871,38 +885,69 @@ TcPlan tc_plan(const tv_attn_args* a) {
   return p;
 }
 
+// Workspace: [split partial outputs][split partial lse][gathered keys (paged caches)].
 size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) {
-  if (p.splits <= 1) return 0;
   const size_t rows = (size_t)a->B * a->Q * a->H;
-  const size_t out_b = ((size_t)p.splits * rows * a->d_latent * 4 + 255) / 256 * 256;
-  const size_t lse_b = ((size_t)p.splits * rows * 4 + 255) / 256 * 256;
-  return out_b + lse_b;
+  size_t n = 0;
+  if (p.splits > 1)
+    n += align256((size_t)p.splits * rows * a->d_latent * 4) + align256((size_t)p.splits * rows * 4);
+  if (a->cache.page_table)
+    n += align256((size_t)a->B * (size_t)gathered_seq_rows(a) * (kDL + kDR) * 2);
+  return n;
 }
 
 cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cudaStream_t st) {
   if (!get_encode()) return cudaErrorNotSupported;
   if (max_clusters() <= 0) return cudaErrorNotSupported;
-  CUtensorMap mc, mk;
-  if (!make_map_latent(&mc, a->c_kv, (uint64_t)a->cache.num_rows, (uint64_t)a->ckv_row_stride * 2))
+  const size_t rows = (size_t)a->B * a->Q * a->H;
+  char* wsp = (char*)ws;
+  float* ws_out = nullptr;
+  float* ws_lse = nullptr;
+  if (pl.splits > 1) {
+    ws_out = (float*)wsp;
+    wsp += align256((size_t)pl.splits * rows * a->d_latent * 4);
+    ws_lse = (float*)wsp;
+    wsp += align256((size_t)pl.splits * rows * 4);
+  }
+  const bool paged = a->cache.page_table != nullptr;
+  const void* lat_base;
+  const void* kpe_base;
+  uint64_t lat_row_bytes, kpe_row_bytes, key_rows;
+  int64_t seq_rows, seq_cap;
+  if (paged) {
+    seq_rows = gathered_seq_rows(a);
+    seq_cap = std::min<int64_t>(seq_rows, (int64_t)a->cache.max_pages * kBN);
+    key_rows = (uint64_t)a->B * (uint64_t)seq_rows;
+    lat_base = wsp;
+    kpe_base = wsp + kDL * 2;
+    lat_row_bytes = kpe_row_bytes = (kDL + kDR) * 2;
+  } else {
+    seq_rows = seq_cap = a->cache.kv_stride_b;
+    key_rows = (uint64_t)a->cache.num_rows;
+    lat_base = a->c_kv;
+    kpe_base = a->k_pe;
+    lat_row_bytes = (uint64_t)a->ckv_row_stride * 2;
+    kpe_row_bytes = (uint64_t)a->kpe_row_stride * 2;
+  }
+  CUtensorMap m_lat_s, m_kpe_s, m_lat_o;
+  if (!make_map_latent(&m_lat_s, lat_base, key_rows, lat_row_bytes, kStep) ||
+      !make_map_rope(&m_kpe_s, kpe_base, key_rows, kpe_row_bytes, kStep) ||
+      !make_map_latent(&m_lat_o, lat_base, key_rows, lat_row_bytes, kBN))
     return cudaErrorInvalidValue;
-  if (!make_map(&mk, a->k_pe, kDR, (uint64_t)a->cache.num_rows, (uint64_t)a->kpe_row_stride * 2))
-    return cudaErrorInvalidValue;
+
   TcParams p{};
   p.q_latent = (const __nv_bfloat16*)a->q_latent;
   p.q_pe = (const __nv_bfloat16*)a->q_pe;
-  p.page_table = a->cache.page_table;
-  p.kv_stride_b = a->cache.kv_stride_b;
+  p.seq_rows = seq_rows;
+  p.seq_cap = seq_cap;
   p.prefix_len = a->prefix_len;
   p.anc = a->anc;
   p.out = a->out;
   p.lse = a->lse;
-  const size_t rows = (size_t)a->B * a->Q * a->H;
-  p.ws_out = (float*)ws;
-  p.ws_lse = ws ? (float*)((char*)ws + ((size_t)pl.splits * rows * a->d_latent * 4 + 255) / 256 * 256)
-                : nullptr;
+  p.ws_out = ws_out;
+  p.ws_lse = ws_lse;
   p.status = a->status;
   p.rows_total = (int64_t)rows;
-  p.max_pages = a->cache.max_pages;
   p.B = a->B;
   p.H = a->H;
   p.Q = a->Q;
@@ -911,9 +956,18 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.splits = pl.splits;
   p.chunk = pl.chunk;
   p.n_items = pl.n_items;
-  p.paged = a->cache.page_table != nullptr;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
   if (p.n_items == 0) return cudaSuccess;
+
+  if (paged) {
+    const dim3 grid((unsigned)(seq_rows / kBN), (unsigned)a->B);
+    gather_kv_kernel<<<grid, 256, 0, st>>>(
+        (const uint4*)a->c_kv, a->ckv_row_stride / 8, (const uint4*)a->k_pe, a->kpe_row_stride / 8,
+        a->cache.page_table, a->cache.max_pages, a->prefix_len, a->Q, a->max_prefix_len,
+        a->cache.num_rows, seq_rows, (uint4*)wsp, a->status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
 
   const int ncl = std::min(pl.clusters, pl.n_items);
   cudaLaunchConfig_t cfg = {};
@@ -928,7 +982,7 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, mc, mk);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o);
   if (e != cudaSuccess || pl.splits == 1) return e;
   return launch_combine(p.ws_out, p.ws_lse, pl.splits, (int64_t)rows, a->d_latent, a->out,
                         a->lse, st);

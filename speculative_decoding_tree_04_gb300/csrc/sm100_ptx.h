@@ -65,13 +65,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// The suspend-time hint (ns) caps how long a waiting thread sleeps inside one probe; a
+// short cap wakes waiters on thread arrivals sooner than the default.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3; "
       "selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
-      : "r"(addr), "r"(parity)
+      : "r"(addr), "r"(parity), "r"(100u)
       : "memory");
   return ok != 0;
 }
@@ -123,6 +125,25 @@ __device__ __forceinline__ void bulk_commit() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Asynchronous stores into a peer CTA's shared memory (cluster addresses).  Each one
+// performs a complete_tx of its size on the peer's mbarrier `bar_cluster` (which must live
+// in the same CTA as the destination); that completion has release semantics at cluster
+// scope, so a thread that waits on the barrier sees the data.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
+                                             uint32_t bar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   cluster_addr),
+               "r"(v), "r"(bar_cluster)
+               : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -227,6 +248,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+// Completion of this thread's earlier tensor-core ops arrives on the barrier at the same
+// shared-memory offset in every CTA of the cluster whose bit is set in cta_mask.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -14,13 +14,15 @@
 // on two SMs that split the two contractions between them:
 //
 //   rank 0 ("S side"): holds the tile's latent queries in TMEM (A operand of QK^T) and
-//     their rope part in shared memory, loads the keys 128 at a time (two 3-D boxes of
-//     4 latent chunks and one rope box), computes S for 128 keys into one of two TMEM
+//     their rope part in shared memory, loads the keys 128 at a time (four 3-D boxes of
+//     2 latent chunks and one rope box), computes S for 128 keys into one of two TMEM
 //     buffers with N = 128 MMAs, runs the masked online softmax (lazy rescaling: the
-//     running max only moves when a block's max exceeds it by more than 2^8), and stores
+//     running max only moves when a block's max exceeds it by more than 2^8), and writes
 //     each 64-key half's P (bf16, in the swizzled K-major layout the MMA reads), the per-row
-//     rescale factor and running row sum straight into rank 1's shared memory with
-//     st.async, whose byte count completes rank 1's inbox barrier.  It writes the lse.
+//     rescale factor and running row sum into a local staging buffer, which one thread
+//     ships to rank 1's inbox with a bulk shared->shared copy (the copy engine streams it
+//     while the softmax goes on; cluster shared-memory traffic runs at only about 21 bytes
+//     per clock, so the softmax threads must not wait on it).  It writes the lse.
 //   rank 1 ("O side"): streams each 64-key block's latent chunks as the V operand
 //     (MN-major B), accumulates O += P V in all 512 TMEM columns, applies the rare
 //     rescales, and at the end of the tile normalises O by the row sums and writes it out.
@@ -28,7 +30,8 @@
 // Per 128 keys the S side issues 36 MMAs of 128x128x16 and the O side 16 of 128x256x16,
 // so the pair is balanced to within 12%.  Warp roles per CTA (256 threads): warp 0 = TMA
 // producer, warp 1 = MMA issuer (and TMEM allocator), warps 4-7 = the row-parallel math
-// (thread = tile row, matching TMEM lanes); warps 2-3 idle.
+// (thread = tile row, matching TMEM lanes; on rank 0 thread 0 of them also issues the
+// message copies); warps 2-3 idle.
 //
 // Keys come from a row-major view of the cache (c_kv row, k_pe row per key).  A 128-key
 // box needs 128 consecutive rows, so a paged cache (64-key pages in any order) is first
@@ -57,23 +60,26 @@ using namespace ptx;
 
 constexpr int kDL = 512, kDR = 64, kBN = 64, kStep = 128, kRows = 128;
 constexpr int kChunkS = kStep * 128;            // 128 keys x 64 bf16 (S side)
-constexpr int kStageS = 4 * kChunkS;            // 4 latent chunks: one 3-D box
-constexpr int kNLS = 3;                         // S-side latent ring stages
+constexpr int kStageS = 2 * kChunkS;            // 2 latent chunks: one 3-D box
+constexpr int kNLS = 4;                         // S-side latent ring stages (one step)
+constexpr int kNRope = 2;                       // S-side rope stages
 constexpr int kChunkO = kBN * 128;              // 64 keys x 64 bf16 (O side)
 constexpr int kHalfO = 4 * kChunkO;             // 4 latent chunks of a 64-key block
 constexpr int kNLO = 4;                         // O-side latent ring stages
 // A message carries one 64-key block: P (128 rows x 64 keys bf16), then per row the
-// rescale factor and running row sum (fp32), then one flags word.
+// rescale factor and running row sum (fp32), then one flags word padded to 16 bytes.
 constexpr int kMsgAlpha = 16384, kMsgL = 16896, kMsgFlags = 17408;
-constexpr uint32_t kMsgBytes = 17412;
-constexpr int kMsgStride = 18432;
+constexpr uint32_t kMsgBytes = 17424;
+constexpr int kMsgStride = 18432;               // inbox buffers (P 1024-byte aligned)
 constexpr int kNInbox = 4;
+constexpr int kNStg = 2;                        // S-side staging buffers (one step)
 constexpr int kThreads = 256;
-// Shared memory, from offset 0 in each CTA.  Rank 0: latent ring, rope stage, the tile's
-// rope queries.  Rank 1: latent ring, inbox.
+// Shared memory, from offset 0 in each CTA.  Rank 0: latent ring, rope stages, the tile's
+// rope queries, staging.  Rank 1: latent ring, inbox.
 constexpr int kRopeOff = kNLS * kStageS;
-constexpr int kQropeOff = kRopeOff + kChunkS;
-constexpr int kSideA = kQropeOff + kRows * 128;
+constexpr int kQropeOff = kRopeOff + kNRope * kChunkS;
+constexpr int kStgOff = kQropeOff + kRows * 128;
+constexpr int kSideA = kStgOff + kNStg * (int)kMsgBytes;
 constexpr int kInboxOff = kNLO * kHalfO;
 constexpr int kSideB = kInboxOff + kNInbox * kMsgStride;
 constexpr int kSmemBytes = (kSideA > kSideB ? kSideA : kSideB) + 1024;
@@ -106,7 +112,7 @@ struct TcParams {
 struct Shared {
   uint64_t slat_full[kNLS], slat_empty[kNLS];
   uint64_t olat_full[kNLO], olat_empty[kNLO];
-  uint64_t rope_full, rope_empty;
+  uint64_t rope_full[kNRope], rope_empty[kNRope];
   uint64_t s_full[2], s_empty[2];
   uint64_t q_ready, q_free, pdst_free[kNInbox];
   uint64_t p_full[kNInbox];
@@ -209,9 +215,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // One 64-key half of a step: p = 2^(s*c - mr) for the 64 scores (masked ones are -inf),
-// packed to bf16 and stored with st.async into the peer's inbox row; returns the sum.
-__device__ __forceinline__ float emit_half(const float* t, float c, float mr, uint32_t row_dst,
-                                           uint32_t sw, uint32_t bar) {
+// packed to bf16 into this row of a staging buffer (swizzled K-major layout); returns the
+// sum.
+__device__ __forceinline__ float emit_half(const float* t, float c, float mr, unsigned char* row,
+                                           uint32_t sw) {
   float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -223,9 +230,19 @@ __device__ __forceinline__ float emit_half(const float* t, float c, float mr, ui
       s4[e] += p0 + p1;
       w[e] = pack_bf16(p0, p1);
     }
-    st_async_v4(row_dst + (((uint32_t)q ^ sw) << 4), w[0], w[1], w[2], w[3], bar);
+    *reinterpret_cast<uint4*>(row + (((uint32_t)q ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
+// Masked keys of a 64-key half get score -inf.
+__device__ __forceinline__ void apply_mask(float* t, uint64_t vis) {
+  if (vis == ~0ull) return;
+  const uint32_t lo = (uint32_t)vis, hi = (uint32_t)(vis >> 32);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) t[k] = ((lo >> k) & 1u) ? t[k] : -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) t[32 + k] = ((hi >> k) & 1u) ? t[32 + k] : -INFINITY;
 }
 
 // ===================================================================================
@@ -241,7 +258,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer: two latent boxes and the rope box per step ---------
+    // ---------------- TMA producer: four latent boxes and the rope box per step --------
     if (lane == 0) {
       prefetch_tensormap(map_lat);
       prefetch_tensormap(map_kpe);
@@ -250,15 +267,16 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         const Item it = decode(p, item);
         for (int j = 0; j < it.ns; ++j, ++rc) {
           const int row0 = (int)key_row(p, it, (int64_t)sweep_step(it, j) * kStep);
-          for (int h = 0; h < 2; ++h, ++u) {
+          for (int h = 0; h < 4; ++h, ++u) {
             const uint32_t st = u % kNLS;
             if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
             mbar_arrive_expect_tx(&sh.slat_full[st], kStageS);
-            tma_load_3d(lat + st * kStageS, map_lat, 0, row0, 4 * h, &sh.slat_full[st]);
+            tma_load_3d(lat + st * kStageS, map_lat, 0, row0, 2 * h, &sh.slat_full[st]);
           }
-          if (!wait_bar(sh, &sh.rope_empty, (rc & 1) ^ 1, p.status)) return;
-          mbar_arrive_expect_tx(&sh.rope_full, kChunkS);
-          tma_load_2d(rope, map_kpe, 0, row0, &sh.rope_full);
+          const uint32_t rs = rc % kNRope;
+          if (!wait_bar(sh, &sh.rope_empty[rs], ((rc / kNRope) & 1) ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.rope_full[rs], kChunkS);
+          tma_load_2d(rope + rs * kChunkS, map_kpe, 0, row0, &sh.rope_full[rs]);
         }
       }
     }
@@ -266,7 +284,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     // ---------------- MMA issuer: S = Q K^T, 128 keys per step ----------------------
     if (lane == 0) {
       uint32_t u = 0, sc = 0, qc = 0, rc = 0;
-      const uint32_t qa = smem_u32(qrope), ra = smem_u32(rope);
+      const uint32_t qa = smem_u32(qrope);
       for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
         const Item it = decode(p, item);
         if (it.ns == 0) continue;
@@ -279,25 +297,27 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           tc_fence_after();  // the softmax warps' TMEM reads of this S buffer come first
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
           bool ok = true;
-          for (int h = 0; h < 2 && ok; ++h, ++u) {
+          for (int h = 0; h < 4 && ok; ++h, ++u) {
             const uint32_t st = u % kNLS;
             if (!wait_bar(sh, &sh.slat_full[st], (u / kNLS) & 1, p.status)) { ok = false; break; }
             const uint32_t sa = smem_u32(lat + st * kStageS);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ts(d, tmem + kTmQ + 32 * (4 * h + c) + 8 * kk,
+                mma_ts(d, tmem + kTmQ + 32 * (2 * h + c) + 8 * kk,
                        smem_desc(sa + c * kChunkS + 32 * kk, 16, 1024, 2), kIdescQK,
                        (h | c | kk) != 0);
             mma_commit(&sh.slat_empty[st]);
           }
-          if (!ok || !wait_bar(sh, &sh.rope_full, rc & 1, p.status)) break;
+          const uint32_t rs = rc % kNRope;
+          if (!ok || !wait_bar(sh, &sh.rope_full[rs], (rc / kNRope) & 1, p.status)) break;
+          const uint32_t ra = smem_u32(rope + rs * kChunkS);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(d, smem_desc(qa + 32 * kk, 16, 1024, 2), smem_desc(ra + 32 * kk, 16, 1024, 2),
                    kIdescQK, 1);
-          mma_commit(&sh.rope_empty);
+          mma_commit(&sh.rope_empty[rs]);
           mma_commit(&sh.s_full[sb]);
         }
         mma_commit(&sh.q_free);
@@ -312,10 +332,12 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const float c = p.scale_log2;
     const uint32_t peer = cluster_rank() ^ 1u;
-    // this row's place in every inbox buffer of the peer, and the buffers' barriers
+    // the peer's inbox; this row's place in a message (swizzled K-major P)
     const uint32_t inbox_peer = map_to_rank(smem_u32(smem + kInboxOff), peer);
+    unsigned char* stg = smem + kStgOff;
     const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
     const uint32_t sw = (uint32_t)(r & 7);
+    bool ok0 = true;  // thread 0: its last inbox waits and copies went through
     // The four warps leave their loops only together, at a 128-thread barrier that agrees
     // on the outcome of the waits before it (a warp that left alone would strand the
     // others at the next barrier).
@@ -427,10 +449,8 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
                  : ((key0 + 2 * kBN > it.P || key0 + 2 * kBN > k1)
                         ? block_vis(key0 + kBN, it.P, k1, anc)
                         : ~0ull);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) t[k] = ((vis0 >> k) & 1ull) ? t[k] : -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) t[64 + k] = ((vis1 >> k) & 1ull) ? t[64 + k] : -INFINITY;
+        apply_mask(t, vis0);
+        apply_mask(t + 64, vis1);
         float mx;
         {
           float a[16];
@@ -453,35 +473,40 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         }
         const float mr = m == -INFINITY ? 0.f : m;
 
-        // ---- wait until the peer's inbox buffers for this step's messages are free ----
-        const uint32_t ib0 = mc % kNInbox, ib1 = (mc + 1) % kNInbox;
-        bool okw = okf && wait_bar(sh, &sh.pdst_free[ib0], ((mc / kNInbox) & 1) ^ 1, p.status);
-        if (two && okw)
-          okw = wait_bar(sh, &sh.pdst_free[ib1], (((mc + 1) / kNInbox) & 1) ^ 1, p.status);
-        // one barrier for the four warps: agree on the outcome and OR the rescale flag
+        // ---- messages: P, alpha, l into the two staging buffers, then bulk copies ----
+        // Thread 0 issued the previous step's copies; once they have read the staging
+        // buffers, the barrier below lets everyone overwrite them.  The barriers also OR
+        // the rescale flag and agree on whether to go on.
+        if (r == 0) bulk_wait_read<0>();
         const bool resc = named_sync_or(1, 128, alpha != 1.f);
-        if (!named_sync_and(2, 128, okw)) {
+        if (!named_sync_and(2, 128, okf && ok0 && !sh.abort)) {
           live = false;
           break;
         }
-
-        const uint32_t dst0 = inbox_peer + ib0 * kMsgStride;
-        const uint32_t bar0 = map_to_rank(smem_u32(&sh.p_full[ib0]), peer);
-        float sum = emit_half(t, c, mr, dst0 + row_off, sw, bar0);
-        uint32_t dst1 = 0, bar1 = 0;
-        if (two) {
-          dst1 = inbox_peer + ib1 * kMsgStride;
-          bar1 = map_to_rank(smem_u32(&sh.p_full[ib1]), peer);
-          sum += emit_half(t + 64, c, mr, dst1 + row_off, sw, bar1);
-        }
+        unsigned char* stg1 = stg + kMsgBytes;
+        float sum = emit_half(t, c, mr, stg + row_off, sw);
+        if (two) sum += emit_half(t + 64, c, mr, stg1 + row_off, sw);
         l = l * alpha + sum;
-        st_async_b32(dst0 + kMsgAlpha + 4 * r, __float_as_uint(alpha), bar0);
-        st_async_b32(dst0 + kMsgL + 4 * r, __float_as_uint(l), bar0);
-        if (r == 0) st_async_b32(dst0 + kMsgFlags, resc ? kFlagRescale : 0u, bar0);
+        reinterpret_cast<float*>(stg + kMsgAlpha)[r] = alpha;
+        reinterpret_cast<float*>(stg + kMsgL)[r] = l;
+        if (r == 0) *reinterpret_cast<uint4*>(stg + kMsgFlags) = make_uint4(resc ? kFlagRescale : 0u, 0u, 0u, 0u);
         if (two) {
-          st_async_b32(dst1 + kMsgAlpha + 4 * r, __float_as_uint(1.f), bar1);
-          st_async_b32(dst1 + kMsgL + 4 * r, __float_as_uint(l), bar1);
-          if (r == 0) st_async_b32(dst1 + kMsgFlags, 0u, bar1);
+          reinterpret_cast<float*>(stg1 + kMsgAlpha)[r] = 1.f;
+          reinterpret_cast<float*>(stg1 + kMsgL)[r] = l;
+          if (r == 0) *reinterpret_cast<uint4*>(stg1 + kMsgFlags) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the bulk copies read the staging through the async proxy
+        named_sync(3, 128);
+        if (r == 0) {
+          // each message goes to the next inbox buffer once rank 1 has released it
+          for (int k = 0; k < (two ? 2 : 1) && ok0; ++k) {
+            const uint32_t mk = mc + k, ib = mk % kNInbox;
+            ok0 = wait_bar(sh, &sh.pdst_free[ib], ((mk / kNInbox) & 1) ^ 1, p.status);
+            if (ok0)
+              bulk_copy_to_cluster(inbox_peer + ib * kMsgStride, stg + k * kMsgBytes, kMsgBytes,
+                                   map_to_rank(smem_u32(&sh.p_full[ib]), peer));
+          }
+          bulk_commit();
         }
         mc += two ? 2 : 1;
       }
@@ -489,6 +514,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       if (vrow && !sh.abort)
         *lse_dst = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
+    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 }
 
@@ -684,8 +710,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
       mbar_init(&sh.olat_full[i], 1);
       mbar_init(&sh.olat_empty[i], 1);
     }
-    mbar_init(&sh.rope_full, 1);
-    mbar_init(&sh.rope_empty, 1);
+    for (int i = 0; i < kNRope; ++i) {
+      mbar_init(&sh.rope_full[i], 1);
+      mbar_init(&sh.rope_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 128);
@@ -780,13 +808,14 @@ bool get_encode() {
   return g_encode != nullptr;
 }
 
-// Latent rows viewed as [64 elements][rows][8 chunks of 64 elements]: one box is 4 chunks
-// of `box_rows` rows, landing chunk-major in shared memory as four 128-byte-swizzled tiles.
+// Latent rows viewed as [64 elements][rows][8 chunks of 64 elements]: one box is
+// `box_chunks` chunks of `box_rows` rows, landing chunk-major in shared memory as
+// 128-byte-swizzled tiles.
 bool make_map_latent(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes,
-                     uint32_t box_rows) {
+                     uint32_t box_rows, uint32_t box_chunks) {
   cuuint64_t dims[3] = {64, rows, kDL / 64};
   cuuint64_t strides[2] = {row_bytes, 128};
-  cuuint32_t box[3] = {64, box_rows, 4};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -930,9 +959,9 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     kpe_row_bytes = (uint64_t)a->kpe_row_stride * 2;
   }
   CUtensorMap m_lat_s, m_kpe_s, m_lat_o;
-  if (!make_map_latent(&m_lat_s, lat_base, key_rows, lat_row_bytes, kStep) ||
+  if (!make_map_latent(&m_lat_s, lat_base, key_rows, lat_row_bytes, kStep, 2) ||
       !make_map_rope(&m_kpe_s, kpe_base, key_rows, kpe_row_bytes, kStep) ||
-      !make_map_latent(&m_lat_o, lat_base, key_rows, lat_row_bytes, kBN))
+      !make_map_latent(&m_lat_o, lat_base, key_rows, lat_row_bytes, kBN, 4))
     return cudaErrorInvalidValue;
 
   TcParams p{};

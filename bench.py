@@ -217,6 +217,8 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (smaller profiler captures)")
     ap.add_argument("--quick", action="store_true",
                     help="device-timed steps only (no end-to-end pass, no CPU baseline); "
                          "used for profiler runs")
@@ -226,7 +228,7 @@ def main():
     from speculative_decoding_tree_04_gb300 import synth
 
     rank, world, local = dist_env()
-    inp = synth.generate(args.workload)
+    inp = synth.generate(args.workload, **({"B": args.batch} if args.batch > 0 else {}))
     if args.impl == "reference":
         run_reference(args, inp, rank, world)
         return

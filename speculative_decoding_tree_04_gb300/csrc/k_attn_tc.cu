@@ -61,8 +61,8 @@ using namespace ptx;
 constexpr int kDL = 512, kDR = 64, kBN = 64, kStep = 128, kRows = 128;
 constexpr int kChunkS = kStep * 128;            // 128 keys x 64 bf16 (S side)
 constexpr int kStageS = 2 * kChunkS;            // 2 latent chunks: one 3-D box
-constexpr int kNLS = 4;                         // S-side latent ring stages (one step)
-constexpr int kNRope = 2;                       // S-side rope stages
+constexpr int kNLS = 5;                         // S-side latent ring stages
+constexpr int kNRope = 1;                       // S-side rope stages
 constexpr int kChunkO = kBN * 128;              // 64 keys x 64 bf16 (O side)
 constexpr int kHalfO = 4 * kChunkO;             // 4 latent chunks of a 64-key block
 constexpr int kNLO = 4;                         // O-side latent ring stages
@@ -82,7 +82,7 @@ constexpr int kStgOff = kQropeOff + kRows * 128;
 constexpr int kSideA = kStgOff + kNStg * (int)kMsgBytes;
 constexpr int kInboxOff = kNLO * kHalfO;
 constexpr int kSideB = kInboxOff + kNInbox * kMsgStride;
-constexpr int kSmemBytes = (kSideA > kSideB ? kSideA : kSideB) + 1024;
+constexpr int kSideMax = kSideA > kSideB ? kSideA : kSideB;
 constexpr uint32_t kTmQ = 0, kTmS0 = 256, kTmS1 = 384;       // S-side TMEM columns
 constexpr uint32_t kFlagRescale = 2;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -106,6 +106,7 @@ struct TcParams {
   int64_t rows_total;  // B*Q*H
   int32_t B, H, Q, max_prefix;
   int32_t tiles_per_seq, splits, chunk, n_items;
+  const int32_t* order;  // (sequence, split) pairs, longest first
   float scale_log2;
 };
 
@@ -122,6 +123,10 @@ struct Shared {
   volatile int job_type, job_buf;
 };
 
+// The barriers live after the buffers in dynamic shared memory (no static shared memory, so
+// the dynamic window starts 1024-byte aligned, as the swizzled tiles need, without padding).
+constexpr int kSmemBytes = kSideMax + (int)((sizeof(Shared) + 15) / 16 * 16);
+
 struct Item {
   int b, t, s, P, nb;
   int ns;   // 128-key steps: ceil(nb / 2)
@@ -130,10 +135,11 @@ struct Item {
   bool bad;
 };
 
+// Work item k of the schedule: tile t of (sequence, split) pair order[k / tiles_per_seq].
 __device__ __noinline__ Item decode(const TcParams& p, int item) {
   Item it;
   it.t = item % p.tiles_per_seq;
-  const int bs = item / p.tiles_per_seq;
+  const int bs = p.order[item / p.tiles_per_seq];
   it.s = bs % p.splits;
   it.b = bs / p.splits;
   it.P = p.prefix_len[it.b];
@@ -149,6 +155,14 @@ __device__ __noinline__ Item decode(const TcParams& p, int item) {
   // request the same cache lines at once (the softmax is independent of block order).
   it.rot = it.ns > 0 ? (int)(((int64_t)it.t * it.ns) / p.tiles_per_seq) : 0;
   return it;
+}
+
+// Item taken by cluster `cid` in round r, or -1 when it has none left.  Items are sorted
+// longest first and dealt out in snake order (rounds alternate direction), which evens
+// out the clusters' total work.
+__device__ __forceinline__ int item_at(const TcParams& p, int r, int cid, int ncl) {
+  const int k = r * ncl + ((r & 1) ? ncl - 1 - cid : cid);
+  return k < p.n_items ? k : -1;
 }
 
 // 128-key step visited at position j of the tile's sweep; it holds the 64-key blocks
@@ -263,7 +277,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       prefetch_tensormap(map_lat);
       prefetch_tensormap(map_kpe);
       uint32_t u = 0, rc = 0;
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+      for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         for (int j = 0; j < it.ns; ++j, ++rc) {
           const int row0 = (int)key_row(p, it, (int64_t)sweep_step(it, j) * kStep);
@@ -285,7 +299,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     if (lane == 0) {
       uint32_t u = 0, sc = 0, qc = 0, rc = 0;
       const uint32_t qa = smem_u32(qrope);
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+      for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         if (it.ns == 0) continue;
         if (!wait_bar(sh, &sh.q_ready, qc & 1, p.status)) break;
@@ -343,7 +357,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     // others at the next barrier).
     uint32_t sc = 0, qc = 0, mc = 0;
     bool live = true;
-    for (int item = cid; item < p.n_items && live; item += ncl) {
+    for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && live; ++rr) {
       const Item it = decode(p, item);
       const int trow = it.t * kRows + r;
       const bool vrow = trow < p.Q * p.H;
@@ -356,8 +370,8 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       }
       {
         // warm L2 with the next tile's queries while this tile runs
-        const int nxt = item + ncl;
-        if (nxt < p.n_items) {
+        const int nxt = item_at(p, rr + 1, cid, ncl);
+        if (nxt >= 0) {
           const Item in = decode(p, nxt);
           const int nrow = in.t * kRows + r;
           if (in.nb > 0 && nrow < p.Q * p.H) {
@@ -534,7 +548,7 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
     if (lane == 0) {
       prefetch_tensormap(map_lat);
       uint32_t u = 0;
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+      for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         for (int j = 0; j < it.ns; ++j) {
           const int st = sweep_step(it, j);
@@ -556,7 +570,7 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
     if (lane == 0) {
       const uint32_t peer = cluster_rank() ^ 1u;
       uint32_t vc = 0, mc = 0, ic = 0, dc = 0, cc = 0, last_pb = 0;
-      for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+      for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         if (it.nb == 0) continue;
         if (ic > 0) {
@@ -625,7 +639,7 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
     const int r = wq * 32 + lane;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     uint32_t jc = 0;
-    for (int item = cid; item < p.n_items && !sh.abort; item += ncl) {
+    for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
       const Item it = decode(p, item);
       const int trow = it.t * kRows + r;
       const bool vrow = trow < p.Q * p.H;
@@ -694,10 +708,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
                const __grid_constant__ CUtensorMap map_kpe_s,
                const __grid_constant__ CUtensorMap map_lat_o) {
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ Shared sh;
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if (smem_u32(smem) & 1023u) {  // both CTAs see the same layout, so both leave here
+    if (threadIdx.x == 0) report(p.status, TV_ERR_UNSUPPORTED);
+    return;
+  }
+  Shared& sh = *reinterpret_cast<Shared*>(smem + kSideMax);
   const uint32_t rank = cluster_rank();
   const int warp = threadIdx.x >> 5;
 
@@ -787,6 +803,37 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
     const uint4 v = w < 64 ? __ldg(ckv + (src0 + i) * ckv_stride16 + w)
                            : __ldg(kpe + (src0 + i) * kpe_stride16 + (w - 64));
     out[(dst0 + i) * kW + w] = v;
+  }
+}
+
+// Orders the (sequence, split) pairs by their number of key blocks, longest first (ties by
+// index), for the snake schedule of the attention kernel.  One CTA ranks all pairs against
+// each other; beyond kMaxRanked pairs the order stays the identity.
+constexpr int kMaxRanked = 1024;
+__global__ void __launch_bounds__(1024)
+schedule_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, int chunk,
+                int max_prefix, int64_t seq_cap, int32_t* __restrict__ order) {
+  __shared__ int cost[kMaxRanked];
+  const int n = B * splits;
+  if (n > kMaxRanked) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = i;
+    return;
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int b = i / splits, sp = i - b * splits;
+    const int P = prefix_len[b];
+    const int64_t kv = (int64_t)P + Q;
+    const int64_t k0 = (int64_t)sp * chunk;
+    const int64_t k1 = k0 + chunk < kv ? k0 + chunk : kv;
+    const bool bad = P < 0 || P > max_prefix || kv > seq_cap;
+    cost[i] = (bad || k1 <= k0) ? 0 : (int)((k1 - k0 + kBN - 1) / kBN);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int ci = cost[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += (cost[j] > ci) || (cost[j] == ci && j < i);
+    order[rank] = i;
   }
 }
 
@@ -914,10 +961,11 @@ TcPlan tc_plan(const tv_attn_args* a) {
   return p;
 }
 
-// Workspace: [split partial outputs][split partial lse][gathered keys (paged caches)].
+// Workspace: [schedule order][split partial outputs][split partial lse][gathered keys
+// (paged caches)].
 size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) {
   const size_t rows = (size_t)a->B * a->Q * a->H;
-  size_t n = 0;
+  size_t n = align256((size_t)a->B * p.splits * 4);
   if (p.splits > 1)
     n += align256((size_t)p.splits * rows * a->d_latent * 4) + align256((size_t)p.splits * rows * 4);
   if (a->cache.page_table)
@@ -930,6 +978,8 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   if (max_clusters() <= 0) return cudaErrorNotSupported;
   const size_t rows = (size_t)a->B * a->Q * a->H;
   char* wsp = (char*)ws;
+  int32_t* order = (int32_t*)wsp;
+  wsp += align256((size_t)a->B * pl.splits * 4);
   float* ws_out = nullptr;
   float* ws_lse = nullptr;
   if (pl.splits > 1) {
@@ -985,9 +1035,12 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.splits = pl.splits;
   p.chunk = pl.chunk;
   p.n_items = pl.n_items;
+  p.order = order;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
   if (p.n_items == 0) return cudaSuccess;
 
+  schedule_kernel<<<1, 1024, 0, st>>>(a->prefix_len, a->B, a->Q, pl.splits, pl.chunk,
+                                      a->max_prefix_len, seq_cap, order);
   if (paged) {
     const dim3 grid((unsigned)(seq_rows / kBN), (unsigned)a->B);
     gather_kv_kernel<<<grid, 256, 0, st>>>(

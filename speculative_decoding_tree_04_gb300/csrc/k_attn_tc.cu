@@ -106,7 +106,7 @@ struct TcParams {
   int64_t rows_total;  // B*Q*H
   int32_t B, H, Q, max_prefix;
   int32_t tiles_per_seq, splits, chunk, n_items;
-  const int32_t* order;  // (sequence, split) pairs, longest first
+  const int4* info;  // per work item: sequence, split, tile, prefix length (longest first)
   float scale_log2;
 };
 
@@ -135,14 +135,15 @@ struct Item {
   bool bad;
 };
 
-// Work item k of the schedule: tile t of (sequence, split) pair order[k / tiles_per_seq].
-__device__ __noinline__ Item decode(const TcParams& p, int item) {
+// Work item k of the schedule, from its record (one 16-byte load).
+__device__ __forceinline__ int4 item_info(const TcParams& p, int item) { return __ldg(p.info + item); }
+
+__device__ __noinline__ Item decode_info(const TcParams& p, int4 v) {
   Item it;
-  it.t = item % p.tiles_per_seq;
-  const int bs = p.order[item / p.tiles_per_seq];
-  it.s = bs % p.splits;
-  it.b = bs / p.splits;
-  it.P = p.prefix_len[it.b];
+  it.b = v.x;
+  it.s = v.y;
+  it.t = v.z;
+  it.P = v.w;
   const int64_t kv_len = (int64_t)it.P + p.Q;
   it.bad = it.P < 0 || it.P > p.max_prefix || kv_len > p.seq_cap;
   it.k0 = (int64_t)it.s * p.chunk;
@@ -155,6 +156,10 @@ __device__ __noinline__ Item decode(const TcParams& p, int item) {
   // request the same cache lines at once (the softmax is independent of block order).
   it.rot = it.ns > 0 ? (int)(((int64_t)it.t * it.ns) / p.tiles_per_seq) : 0;
   return it;
+}
+
+__device__ __forceinline__ Item decode(const TcParams& p, int item) {
+  return decode_info(p, item_info(p, item));
 }
 
 // Item taken by cluster `cid` in round r, or -1 when it has none left.  Items are sorted
@@ -249,6 +254,23 @@ __device__ __forceinline__ float emit_half(const float* t, float c, float mr, un
   return (s4[0] + s4[1]) + (s4[2] + s4[3]);
 }
 
+// Two 32-column chunks of a row's latent queries (16 x 16 bytes) into TMEM at `taddr`.
+__device__ __forceinline__ void store_q_chunks(uint32_t taddr, const uint4* v) {
+  uint32_t w[2][32];
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      w[cc][4 * e + 0] = v[8 * cc + e].x;
+      w[cc][4 * e + 1] = v[8 * cc + e].y;
+      w[cc][4 * e + 2] = v[8 * cc + e].z;
+      w[cc][4 * e + 3] = v[8 * cc + e].w;
+    }
+  __syncwarp();
+  tmem_st32(taddr, w[0]);
+  tmem_st32(taddr + 32, w[1]);
+}
+
 // Masked keys of a 64-key half get score -inf.
 __device__ __forceinline__ void apply_mask(float* t, uint64_t vis) {
   if (vis == ~0ull) return;
@@ -298,7 +320,10 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     // ---------------- MMA issuer: S = Q K^T, 128 keys per step ----------------------
     if (lane == 0) {
       uint32_t u = 0, sc = 0, qc = 0, rc = 0;
-      const uint32_t qa = smem_u32(qrope);
+      // descriptors are formed once per stage; the MMAs of a stage add constant offsets
+      // (address bits 4..17 sit in the low field, which these offsets never overflow)
+      const uint64_t dq = smem_desc(smem_u32(qrope), 16, 1024, 2);
+      const uint64_t dr = smem_desc(smem_u32(rope), 16, 1024, 2);
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         if (it.ns == 0) continue;
@@ -311,26 +336,25 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           tc_fence_after();  // the softmax warps' TMEM reads of this S buffer come first
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
           bool ok = true;
-          for (int h = 0; h < 4 && ok; ++h, ++u) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h, ++u) {
             const uint32_t st = u % kNLS;
             if (!wait_bar(sh, &sh.slat_full[st], (u / kNLS) & 1, p.status)) { ok = false; break; }
-            const uint32_t sa = smem_u32(lat + st * kStageS);
+            const uint64_t db = smem_desc(smem_u32(lat + st * kStageS), 16, 1024, 2);
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 mma_ts(d, tmem + kTmQ + 32 * (2 * h + c) + 8 * kk,
-                       smem_desc(sa + c * kChunkS + 32 * kk, 16, 1024, 2), kIdescQK,
-                       (h | c | kk) != 0);
+                       db + (uint64_t)((c * kChunkS + 32 * kk) >> 4), kIdescQK, (h | c | kk) != 0);
             mma_commit(&sh.slat_empty[st]);
           }
           const uint32_t rs = rc % kNRope;
           if (!ok || !wait_bar(sh, &sh.rope_full[rs], (rc / kNRope) & 1, p.status)) break;
-          const uint32_t ra = smem_u32(rope + rs * kChunkS);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(d, smem_desc(qa + 32 * kk, 16, 1024, 2), smem_desc(ra + 32 * kk, 16, 1024, 2),
-                   kIdescQK, 1);
+            mma_ss(d, dq + (uint64_t)((32 * kk) >> 4),
+                   dr + (uint64_t)((rs * kChunkS + 32 * kk) >> 4), kIdescQK, 1);
           mma_commit(&sh.rope_empty[rs]);
           mma_commit(&sh.s_full[sb]);
         }
@@ -357,8 +381,14 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     // others at the next barrier).
     uint32_t sc = 0, qc = 0, mc = 0;
     bool live = true;
-    for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && live; ++rr) {
-      const Item it = decode(p, item);
+    // The next item's record is requested a whole tile ahead, so that at a tile boundary
+    // only the query loads stand between the last step and the next tile's first MMAs.
+    int item_next = item_at(p, 0, cid, ncl);
+    int4 info_next = item_next >= 0 ? item_info(p, item_next) : make_int4(0, 0, 0, 0);
+    for (int rr = 0; item_next >= 0 && live; ++rr) {
+      const Item it = decode_info(p, info_next);
+      item_next = item_at(p, rr + 1, cid, ncl);
+      if (item_next >= 0) info_next = item_info(p, item_next);
       const int trow = it.t * kRows + r;
       const bool vrow = trow < p.Q * p.H;
       const int64_t grow = (int64_t)it.b * p.Q * p.H + trow;
@@ -368,66 +398,58 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         if (vrow) *lse_dst = -INFINITY;
         continue;
       }
-      {
-        // warm L2 with the next tile's queries while this tile runs
-        const int nxt = item_at(p, rr + 1, cid, ncl);
-        if (nxt >= 0) {
-          const Item in = decode(p, nxt);
-          const int nrow = in.t * kRows + r;
-          if (in.nb > 0 && nrow < p.Q * p.H) {
-            const int64_t ng = (int64_t)in.b * p.Q * p.H + nrow;
-            const char* qlp = reinterpret_cast<const char*>(p.q_latent + ng * kDL);
-#pragma unroll
-            for (int l128 = 0; l128 < 8; ++l128) prefetch_l2(qlp + 128 * l128);
-            prefetch_l2(p.q_pe + ng * kDR);
-          }
-        }
-      }
       const uint64_t anc = vrow ? p.anc[(int64_t)it.b * p.Q + trow / p.H] : 0ull;
       const int64_t kv_end = (int64_t)it.P + p.Q;
       const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
 
       // ---- latent queries into TMEM columns [0, 256), rope queries into shared memory ----
-      if (!named_sync_and(3, 128, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) {
-        live = false;
-        break;
-      }
-      ++qc;
-      tc_fence_after();
+      // The loads are software-pipelined two chunks (32 columns each) at a time, and the
+      // first four chunks and the rope part are requested before waiting for the previous
+      // tile's MMAs to release the query storage.
       {
         const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + grow * kDL);
         const uint4* qr = reinterpret_cast<const uint4*>(p.q_pe + grow * kDR);
-#pragma unroll 1
-        for (int c0 = 0; c0 < 8; c0 += 2) {
-          uint32_t w[2][32];
+        uint4 qa[16], qb[16], qp[8];
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
+        for (int e = 0; e < 16; ++e) qa[e] = vrow ? __ldg(ql + e) : z;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (vrow) v = __ldg(ql + 8 * (c0 + cc) + e);
-              w[cc][4 * e + 0] = v.x;
-              w[cc][4 * e + 1] = v.y;
-              w[cc][4 * e + 2] = v.z;
-              w[cc][4 * e + 3] = v.w;
-            }
-          }
-          __syncwarp();
+        for (int e = 0; e < 16; ++e) qb[e] = vrow ? __ldg(ql + 16 + e) : z;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) tmem_st32(tmem + lane_base + kTmQ + 32 * (c0 + cc), w[cc]);
+        for (int e = 0; e < 8; ++e) qp[e] = vrow ? __ldg(qr + e) : z;
+        if (!named_sync_and(3, 128, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) {
+          live = false;
+          break;
         }
+        ++qc;
+        tc_fence_after();
+        store_q_chunks(tmem + lane_base + kTmQ, qa);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qa[e] = vrow ? __ldg(ql + 32 + e) : z;
+        store_q_chunks(tmem + lane_base + kTmQ + 64, qb);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qb[e] = vrow ? __ldg(ql + 48 + e) : z;
         unsigned char* qrow = qrope + row_off;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (vrow) v = __ldg(qr + e);
-          *reinterpret_cast<uint4*>(qrow + (((uint32_t)e ^ sw) << 4)) = v;
-        }
+        for (int e = 0; e < 8; ++e) *reinterpret_cast<uint4*>(qrow + (((uint32_t)e ^ sw) << 4)) = qp[e];
+        store_q_chunks(tmem + lane_base + kTmQ + 128, qa);
+        store_q_chunks(tmem + lane_base + kTmQ + 192, qb);
       }
       tmem_wait_st();
       fence_proxy_async_smem();  // the rope queries are read by the MMAs
       tc_fence_before();
       mbar_arrive(&sh.q_ready);
+      if (item_next >= 0) {
+        // warm L2 with the next tile's queries while this tile runs
+        const int nrow = info_next.z * kRows + r;
+        if (nrow < p.Q * p.H) {
+          const int64_t ng = (int64_t)info_next.x * p.Q * p.H + nrow;
+          const char* qlp = reinterpret_cast<const char*>(p.q_latent + ng * kDL);
+#pragma unroll
+          for (int l128 = 0; l128 < 8; ++l128) prefetch_l2(qlp + 128 * l128);
+          prefetch_l2(p.q_pe + ng * kDR);
+        }
+      }
 
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.ns; ++j, ++sc) {
@@ -807,19 +829,18 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
 }
 
 // Orders the (sequence, split) pairs by their number of key blocks, longest first (ties by
-// index), for the snake schedule of the attention kernel.  One CTA ranks all pairs against
-// each other; beyond kMaxRanked pairs the order stays the identity.
+// index), for the snake schedule of the attention kernel, and writes one record per work
+// item.  One CTA ranks all pairs against each other; beyond kMaxRanked pairs the order
+// stays the identity.
 constexpr int kMaxRanked = 1024;
 __global__ void __launch_bounds__(1024)
 schedule_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, int chunk,
-                int max_prefix, int64_t seq_cap, int32_t* __restrict__ order) {
+                int max_prefix, int64_t seq_cap, int tiles, int n_items, int4* __restrict__ info) {
   __shared__ int cost[kMaxRanked];
+  __shared__ int order[kMaxRanked];
   const int n = B * splits;
-  if (n > kMaxRanked) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) order[i] = i;
-    return;
-  }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  const bool ranked = n <= kMaxRanked;
+  for (int i = threadIdx.x; ranked && i < n; i += blockDim.x) {
     const int b = i / splits, sp = i - b * splits;
     const int P = prefix_len[b];
     const int64_t kv = (int64_t)P + Q;
@@ -829,11 +850,19 @@ schedule_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits
     cost[i] = (bad || k1 <= k0) ? 0 : (int)((k1 - k0 + kBN - 1) / kBN);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int i = threadIdx.x; ranked && i < n; i += blockDim.x) {
     const int ci = cost[i];
     int rank = 0;
     for (int j = 0; j < n; ++j) rank += (cost[j] > ci) || (cost[j] == ci && j < i);
     order[rank] = i;
+  }
+  __syncthreads();
+  // item k: tile k % tiles of pair order[k / tiles]
+  for (int k = threadIdx.x; k < n_items; k += blockDim.x) {
+    const int q = k / tiles;
+    const int pair = ranked ? order[q] : q;
+    const int b = pair / splits;
+    info[k] = make_int4(b, pair - b * splits, k - q * tiles, prefix_len[b]);
   }
 }
 
@@ -961,11 +990,11 @@ TcPlan tc_plan(const tv_attn_args* a) {
   return p;
 }
 
-// Workspace: [schedule order][split partial outputs][split partial lse][gathered keys
+// Workspace: [work-item records][split partial outputs][split partial lse][gathered keys
 // (paged caches)].
 size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) {
   const size_t rows = (size_t)a->B * a->Q * a->H;
-  size_t n = align256((size_t)a->B * p.splits * 4);
+  size_t n = align256((size_t)p.n_items * 16);
   if (p.splits > 1)
     n += align256((size_t)p.splits * rows * a->d_latent * 4) + align256((size_t)p.splits * rows * 4);
   if (a->cache.page_table)
@@ -978,8 +1007,8 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   if (max_clusters() <= 0) return cudaErrorNotSupported;
   const size_t rows = (size_t)a->B * a->Q * a->H;
   char* wsp = (char*)ws;
-  int32_t* order = (int32_t*)wsp;
-  wsp += align256((size_t)a->B * pl.splits * 4);
+  int4* info = (int4*)wsp;
+  wsp += align256((size_t)pl.n_items * 16);
   float* ws_out = nullptr;
   float* ws_lse = nullptr;
   if (pl.splits > 1) {
@@ -1035,12 +1064,13 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.splits = pl.splits;
   p.chunk = pl.chunk;
   p.n_items = pl.n_items;
-  p.order = order;
+  p.info = info;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
   if (p.n_items == 0) return cudaSuccess;
 
   schedule_kernel<<<1, 1024, 0, st>>>(a->prefix_len, a->B, a->Q, pl.splits, pl.chunk,
-                                      a->max_prefix_len, seq_cap, order);
+                                      a->max_prefix_len, seq_cap, pl.tiles_per_seq, pl.n_items,
+                                      info);
   if (paged) {
     const dim3 grid((unsigned)(seq_rows / kBN), (unsigned)a->B);
     gather_kv_kernel<<<grid, 256, 0, st>>>(

@@ -215,6 +215,14 @@ __device__ __forceinline__ bool wait_bar(Shared& sh, uint64_t* bar, uint32_t par
   return wait_bar_slow(sh, a, parity, status);
 }
 
+// Same, for a barrier that only this CTA's threads, TMA loads and MMAs complete.
+__device__ __forceinline__ bool wait_bar_cta(Shared& sh, uint64_t* bar, uint32_t parity,
+                                             int32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cta(a, parity)) return true;
+  return wait_bar_slow(sh, a, parity, status);
+}
+
 // Visibility of keys key0 .. key0+63 for a row whose node has ancestor bitset `anc`: bit k
 // set iff key0 + k < k1 and (key0 + k is a prefix key, or the tree node key0 + k - P is an
 // ancestor-or-self of the row's node).
@@ -319,11 +327,15 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
   } else if (warp == 1) {
     // ---------------- MMA issuer: S = Q K^T, 128 keys per step ----------------------
     if (lane == 0) {
-      uint32_t u = 0, sc = 0, qc = 0, rc = 0;
-      // descriptors are formed once per stage; the MMAs of a stage add constant offsets
-      // (address bits 4..17 sit in the low field, which these offsets never overflow)
+      // The issuing thread must keep the tensor pipe's queue fed, so its loop is kept lean:
+      // stage index, phase and descriptor advance incrementally, and the MMAs of a stage
+      // add constant offsets to one descriptor (address bits 4..17 sit in its low field,
+      // which these offsets never overflow).
+      uint32_t sc = 0, qc = 0, rc = 0, st = 0, sph = 0;
       const uint64_t dq = smem_desc(smem_u32(qrope), 16, 1024, 2);
       const uint64_t dr = smem_desc(smem_u32(rope), 16, 1024, 2);
+      const uint64_t dl0 = smem_desc(smem_u32(lat), 16, 1024, 2);
+      uint64_t db = dl0;
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         if (it.ns == 0) continue;
@@ -332,15 +344,13 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         tc_fence_after();
         for (int j = 0; j < it.ns && !sh.abort; ++j, ++sc, ++rc) {
           const uint32_t sb = sc & 1;
-          if (!wait_bar(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
+          if (!wait_bar_cta(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
           tc_fence_after();  // the softmax warps' TMEM reads of this S buffer come first
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
           bool ok = true;
 #pragma unroll
-          for (int h = 0; h < 4; ++h, ++u) {
-            const uint32_t st = u % kNLS;
-            if (!wait_bar(sh, &sh.slat_full[st], (u / kNLS) & 1, p.status)) { ok = false; break; }
-            const uint64_t db = smem_desc(smem_u32(lat + st * kStageS), 16, 1024, 2);
+          for (int h = 0; h < 4; ++h) {
+            if (!wait_bar_cta(sh, &sh.slat_full[st], sph, p.status)) { ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -348,14 +358,19 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
                 mma_ts(d, tmem + kTmQ + 32 * (2 * h + c) + 8 * kk,
                        db + (uint64_t)((c * kChunkS + 32 * kk) >> 4), kIdescQK, (h | c | kk) != 0);
             mma_commit(&sh.slat_empty[st]);
+            db += kStageS >> 4;
+            if (++st == kNLS) {
+              st = 0;
+              sph ^= 1;
+              db = dl0;
+            }
           }
-          const uint32_t rs = rc % kNRope;
-          if (!ok || !wait_bar(sh, &sh.rope_full[rs], (rc / kNRope) & 1, p.status)) break;
+          static_assert(kNRope == 1, "one rope stage");
+          if (!ok || !wait_bar_cta(sh, &sh.rope_full[0], rc & 1, p.status)) break;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(d, dq + (uint64_t)((32 * kk) >> 4),
-                   dr + (uint64_t)((rs * kChunkS + 32 * kk) >> 4), kIdescQK, 1);
-          mma_commit(&sh.rope_empty[rs]);
+            mma_ss(d, dq + (uint64_t)((32 * kk) >> 4), dr + (uint64_t)((32 * kk) >> 4), kIdescQK, 1);
+          mma_commit(&sh.rope_empty[0]);
           mma_commit(&sh.s_full[sb]);
         }
         mma_commit(&sh.q_free);

@@ -246,20 +246,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // sum.
 __device__ __forceinline__ float emit_half(const float* t, float c, float mr, unsigned char* row,
                                            uint32_t sw) {
-  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint64_t cc = f2_pack(c, c), nm = f2_pack(-mr, -mr);
+  uint64_t s2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float p0 = ex2(fmaf(t[8 * q + 2 * e], c, -mr));
-      const float p1 = ex2(fmaf(t[8 * q + 2 * e + 1], c, -mr));
-      s4[e] += p0 + p1;
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(t[8 * q + 2 * e], t[8 * q + 2 * e + 1]), cc, nm), x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      s2[e & 1] = f2_add(s2[e & 1], f2_pack(p0, p1));
       w[e] = pack_bf16(p0, p1);
     }
     *reinterpret_cast<uint4*>(row + (((uint32_t)q ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+  float a0, a1, b0, b1;
+  f2_unpack(s2[0], a0, a1);
+  f2_unpack(s2[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
 }
 
 // Two 32-column chunks of a row's latent queries (16 x 16 bytes) into TMEM at `taddr`.
@@ -504,16 +509,17 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         apply_mask(t + 64, vis1);
         float mx;
         {
-          float a[16];
+          // 128 -> 43 -> 15 -> 5 -> 2 -> 1 with three-input maxima
+          float a[43];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            a[i] = fmaxf(fmaxf(fmaxf(t[8 * i], t[8 * i + 1]), fmaxf(t[8 * i + 2], t[8 * i + 3])),
-                         fmaxf(fmaxf(t[8 * i + 4], t[8 * i + 5]), fmaxf(t[8 * i + 6], t[8 * i + 7])));
+          for (int i = 0; i < 42; ++i) a[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+          a[42] = fmaxf(t[126], t[127]);
 #pragma unroll
-          for (int w = 8; w >= 1; w >>= 1)
+          for (int i = 0; i < 14; ++i) a[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+          a[14] = a[42];
 #pragma unroll
-            for (int i = 0; i < w; ++i) a[i] = fmaxf(a[i], a[i + w]);
-          mx = a[0] * c;  // block max of score*scale in log2 units (-inf if all masked)
+          for (int i = 0; i < 5; ++i) a[i] = fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+          mx = fmax3(a[0], a[1], fmaxf(a[2], fmaxf(a[3], a[4]))) * c;  // block max in log2 units
         }
         // The running max m moves only when the block max exceeds it by more than 2^8;
         // then O and l are rescaled by alpha = 2^(m_old - m_new).

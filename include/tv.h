@@ -171,12 +171,20 @@ typedef struct {
 } tv_attn_args;
 
 /* Bytes of workspace tv_verify_attn needs for these arguments (0 if none).  The size
- * depends on B, H, Q, d_latent, max_prefix_len, the path and num_splits only. */
+ * depends on B, H, Q, d_latent, max_prefix_len, whether the cache is paged, the path and
+ * num_splits only (the tensor-core path of a paged cache also keeps a contiguous copy of
+ * the keys there). */
 size_t tv_verify_attn_workspace_size(const tv_attn_args* a);
 
 /* The kernel family TV_PATH_AUTO resolves to for these arguments, or a negative
  * tv_status if the arguments are invalid. */
 int tv_verify_attn_path(const tv_attn_args* a);
+
+/* How many kernels one tv_verify_attn call with these arguments enqueues (for launch
+ * accounting; the CUDA-core path: attention + split combine; the tensor-core path: work
+ * schedule + key gather for a paged cache + attention + split combine), or a negative
+ * tv_status if the arguments are invalid. */
+int tv_verify_attn_launches(const tv_attn_args* a);
 
 /*
  * tv_verify_attn -- run the attention.  workspace: device memory of at least

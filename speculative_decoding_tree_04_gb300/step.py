@@ -104,8 +104,8 @@ class VerifyStep:
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        """Kernels one run() enqueues: visibility, 2 RoPE, attention (+ combine if split)."""
-        return 4 + (1 if self.workspace is not None else 0)
+        """Kernels one run() enqueues: visibility, 2 RoPE, and the attention call's own."""
+        return 3 + tv.attn_launches(self.attn_args())
 
     # -- results --------------------------------------------------------------------
     def results(self):

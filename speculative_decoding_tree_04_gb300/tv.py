@@ -79,6 +79,7 @@ def load():
     lib.tv_verify_attn_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
     lib.tv_verify_attn_workspace_size.restype = ctypes.c_size_t
     lib.tv_verify_attn_path.argtypes = [ctypes.POINTER(AttnArgs)]
+    lib.tv_verify_attn_launches.argtypes = [ctypes.POINTER(AttnArgs)]
     lib.tv_verify_attn.argtypes = [ctypes.POINTER(AttnArgs), P, ctypes.c_size_t, P]
     lib.tv_verify_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), P]
     lib.tv_noalloc_scratch_bytes.restype = ctypes.c_size_t
@@ -211,6 +212,14 @@ def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_
 
 def workspace_size(a: AttnArgs) -> int:
     return int(load().tv_verify_attn_workspace_size(ctypes.byref(a)))
+
+
+def attn_launches(a: AttnArgs) -> int:
+    """Kernels one tv_verify_attn call with these arguments enqueues."""
+    rc = load().tv_verify_attn_launches(ctypes.byref(a))
+    if rc < 0:
+        _check(rc, "tv_verify_attn_launches")
+    return rc
 
 
 def chosen_path(a: AttnArgs) -> int:

@@ -107,6 +107,7 @@ struct TcParams {
   int32_t B, H, Q, max_prefix;
   int32_t tiles_per_seq, splits, chunk, n_items;
   const int4* info;  // per work item: sequence, split, tile, prefix length (longest first)
+  int32_t wait_all;  // 1: the records come from the kernel just before (wait before any read)
   float scale_log2;
 };
 
@@ -309,6 +310,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
   if (warp == 0) {
     // ---------------- TMA producer: four latent boxes and the rope box per step --------
     if (lane == 0) {
+      griddep_wait();  // the key view may still be being written by the gather kernel
       prefetch_tensormap(map_lat);
       prefetch_tensormap(map_kpe);
       uint32_t u = 0, rc = 0;
@@ -589,6 +591,7 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
   if (warp == 0) {
     // ---------------- TMA producer: each 64-key block's latent chunks, in message order --
     if (lane == 0) {
+      griddep_wait();  // the key view may still be being written by the gather kernel
       prefetch_tensormap(map_lat);
       uint32_t u = 0;
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
@@ -757,6 +760,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
     return;
   }
   Shared& sh = *reinterpret_cast<Shared*>(smem + kSideMax);
+  // The kernel may start while the kernel before it in the stream still runs (programmatic
+  // dependent launch).  Everything written before that kernel is visible; its own output
+  // (the key view, or the work records when no gather runs) is waited for before use.
+  if (p.wait_all) griddep_wait();
   const uint32_t rank = cluster_rank();
   const int warp = threadIdx.x >> 5;
 
@@ -829,6 +836,7 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
                  const int32_t* __restrict__ prefix_len, int Q, int max_prefix, int64_t num_rows,
                  int64_t seq_rows, uint4* __restrict__ out, int32_t* status) {
   constexpr int kW = (kDL + kDR) * 2 / 16;  // 72 16-byte words per key row
+  griddep_launch_dependents();  // the attention kernel may start its prologue now
   const int b = blockIdx.y, j = blockIdx.x;
   const int P = prefix_len[b];
   if (P < 0 || P > max_prefix) return;  // reported by the attention kernel
@@ -859,6 +867,7 @@ schedule_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits
                 int max_prefix, int64_t seq_cap, int tiles, int n_items, int4* __restrict__ info) {
   __shared__ int cost[kMaxRanked];
   __shared__ int order[kMaxRanked];
+  griddep_launch_dependents();  // a following attention kernel waits for these records
   const int n = B * splits;
   const bool ranked = n <= kMaxRanked;
   for (int i = threadIdx.x; ranked && i < n; i += blockDim.x) {
@@ -1086,6 +1095,7 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.chunk = pl.chunk;
   p.n_items = pl.n_items;
   p.info = info;
+  p.wait_all = paged ? 0 : 1;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
   if (p.n_items == 0) return cudaSuccess;
 
@@ -1108,13 +1118,15 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o);
   if (e != cudaSuccess || pl.splits == 1) return e;
   return launch_combine(p.ws_out, p.ws_lse, pl.splits, (int64_t)rows, a->d_latent, a->out,

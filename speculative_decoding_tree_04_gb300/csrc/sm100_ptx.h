@@ -45,6 +45,17 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------
+// Wait until the grid this one depends on (the previous kernel in the stream, when this one
+// was launched with programmatic stream serialisation) has finished and its memory is
+// visible; returns at once otherwise.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream (if launched with programmatic stream serialisation)
+// start before this grid finishes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier -----------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));

@@ -461,20 +461,21 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       fence_proxy_async_smem();  // the rope queries are read by the MMAs
       tc_fence_before();
       mbar_arrive(&sh.q_ready);
-      if (item_next >= 0) {
-        // warm L2 with the next tile's queries while this tile runs
-        const int nrow = info_next.z * kRows + r;
-        if (nrow < p.Q * p.H) {
-          const int64_t ng = (int64_t)info_next.x * p.Q * p.H + nrow;
-          const char* qlp = reinterpret_cast<const char*>(p.q_latent + ng * kDL);
-#pragma unroll
-          for (int l128 = 0; l128 < 8; ++l128) prefetch_l2(qlp + 128 * l128);
-          prefetch_l2(p.q_pe + ng * kDR);
-        }
-      }
 
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.ns; ++j, ++sc) {
+        if (j == (it.ns > 3 ? it.ns - 3 : 0) && item_next >= 0) {
+          // warm L2 with the next tile's queries a few steps before they are needed (the
+          // key stream would evict lines fetched much earlier)
+          const int nrow = info_next.z * kRows + r;
+          if (nrow < p.Q * p.H) {
+            const int64_t ng = (int64_t)info_next.x * p.Q * p.H + nrow;
+            const char* qlp = reinterpret_cast<const char*>(p.q_latent + ng * kDL);
+#pragma unroll
+            for (int l128 = 0; l128 < 8; ++l128) prefetch_l2(qlp + 128 * l128);
+            prefetch_l2(p.q_pe + ng * kDR);
+          }
+        }
         const uint32_t sb = sc & 1;
         // each warp agrees before its warp-collective TMEM loads
         const bool okf =

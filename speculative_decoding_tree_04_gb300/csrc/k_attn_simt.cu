@@ -307,35 +307,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(const SimtArgs a
   }
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ ws_out,
+// One warp per row.  Lane s < splits forms split s's weight; the weights are then summed
+// and applied in split order (the same arithmetic per element as a serial merge), each
+// lane merging four float4 columns at a time so that their loads overlap.  More than 32
+// splits take a plain serial merge.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_out,
                                                       const float* __restrict__ ws_lse,
                                                       int splits, int64_t rows, int DL,
                                                       float* __restrict__ out,
                                                       float* __restrict__ lse) {
-  const int64_t row = blockIdx.x;
-  float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, ws_lse[(int64_t)s * rows + row]);
-  float wsum = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float ls = ws_lse[(int64_t)s * rows + row];
-    wsum += (mx == -INFINITY) ? 0.f : expf(ls - mx);
-  }
-  const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-  for (int d4 = threadIdx.x; d4 < DL / 4; d4 += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  if (splits > 32) {  // many splits (forced by the caller): plain serial merge
+    float m = -INFINITY;
+    for (int s = 0; s < splits; ++s) m = fmaxf(m, ws_lse[(int64_t)s * rows + row]);
+    float sum = 0.f;
     for (int s = 0; s < splits; ++s) {
-      const float ls = ws_lse[(int64_t)s * rows + row];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - mx) * winv;
-      const float4 v = *(const float4*)(ws_out + ((int64_t)s * rows + row) * DL + 4 * d4);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+      const float l = ws_lse[(int64_t)s * rows + row];
+      sum += (m == -INFINITY) ? 0.f : expf(l - m);
     }
-    *(float4*)(out + row * DL + 4 * d4) = acc;
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    for (int d4 = lane; d4 < DL / 4; d4 += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < splits; ++s) {
+        const float l = ws_lse[(int64_t)s * rows + row];
+        if (l == -INFINITY) continue;
+        const float wt = expf(l - m) * inv;
+        const float4 v = *(const float4*)(ws_out + ((int64_t)s * rows + row) * DL + 4 * d4);
+        acc.x = fmaf(wt, v.x, acc.x);
+        acc.y = fmaf(wt, v.y, acc.y);
+        acc.z = fmaf(wt, v.z, acc.z);
+        acc.w = fmaf(wt, v.w, acc.w);
+      }
+      *(float4*)(out + row * DL + 4 * d4) = acc;
+    }
+    if (lane == 0) lse[row] = sum > 0.f ? m + logf(sum) : -INFINITY;
+    return;
   }
-  if (threadIdx.x == 0) lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+  const float ls = lane < splits ? ws_lse[(int64_t)lane * rows + row] : -INFINITY;
+  float mx = ls;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float e = (lane < splits && mx != -INFINITY) ? expf(ls - mx) : 0.f;
+  float wsum = 0.f;
+  for (int s = 0; s < splits; ++s) wsum += __shfl_sync(0xffffffffu, e, s);
+  const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float w = e * winv;
+  const int n4 = DL / 4;
+  for (int base = 0; base < n4; base += 128) {
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < splits; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      const float lss = __shfl_sync(0xffffffffu, ls, s);
+      if (lss == -INFINITY) continue;  // uniform over the warp
+      const float4* src = (const float4*)(ws_out + ((int64_t)s * rows + row) * DL);
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int d4 = base + lane + 32 * i;
+        v[i] = d4 < n4 ? src[d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i].x = fmaf(ws, v[i].x, acc[i].x);
+        acc[i].y = fmaf(ws, v[i].y, acc[i].y);
+        acc[i].z = fmaf(ws, v[i].z, acc[i].z);
+        acc[i].w = fmaf(ws, v[i].w, acc[i].w);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int d4 = base + lane + 32 * i;
+      if (d4 < n4) *(float4*)(out + row * DL + 4 * d4) = acc[i];
+    }
+  }
+  if (lane == 0) lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 template <typename T, int TMAX, int VMAX>
@@ -452,7 +501,8 @@ cudaError_t launch_attn_simt(const tv_attn_args* a, const SimtPlan& p, void* ws,
 cudaError_t launch_combine(const float* ws_out, const float* ws_lse, int splits, int64_t rows,
                            int DL, float* out, float* lse, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  combine_kernel<<<(unsigned)rows, 128, 0, st>>>(ws_out, ws_lse, splits, rows, DL, out, lse);
+  combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(ws_out, ws_lse, splits, rows, DL,
+                                                              out, lse);
   return cudaGetLastError();
 }
 

@@ -1002,13 +1002,29 @@ TcPlan tc_plan(const tv_attn_args* a) {
   const int64_t tiles = (int64_t)a->B * p.tiles_per_seq;
   const int64_t kv_max = (int64_t)a->max_prefix_len + a->Q;
   int splits = a->num_splits;
-  if (splits <= 0) {
+  if (splits <= 0 && tiles < clusters) {
+    // Fewer tiles than clusters: split the keys.  Pick the count that minimises a simple
+    // makespan model -- items of the longest length dealt to the clusters in rounds, each
+    // costing a tile start-up (about two 128-key steps on this GPU) plus its steps, plus
+    // the combine pass (its HBM bytes at ~6 TB/s, in units of a ~2.4 us step, and one
+    // launch).
     splits = 1;
-    if (tiles < 2LL * clusters) {
-      const int64_t want = (2LL * clusters + tiles - 1) / std::max<int64_t>(tiles, 1);
-      const int64_t cap = std::max<int64_t>(1, kv_max / 512);
-      splits = (int)std::max<int64_t>(1, std::min(want, cap));
+    const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(16, kv_max / 256));
+    const double rows = (double)a->B * a->Q * a->H;
+    double best = 1e30;
+    for (int64_t s = 1; s <= cap; ++s) {
+      const int64_t items = tiles * s;
+      const int64_t rounds = (items + clusters - 1) / clusters;
+      const int64_t steps = ((kv_max + s - 1) / s + kStep - 1) / kStep;
+      const double comb_us = rows * (double)(s + 1) * a->d_latent * 4.0 / 6.0e6;
+      const double t = (double)rounds * (2.0 + (double)steps) + (s > 1 ? 1.0 + comb_us / 2.4 : 0.0);
+      if (t < best - 1e-9) {
+        best = t;
+        splits = (int)s;
+      }
     }
+  } else if (splits <= 0) {
+    splits = 1;
   }
   // split boundaries fall on whole 128-key steps
   int64_t chunk = (kv_max + splits - 1) / splits;

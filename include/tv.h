@@ -182,8 +182,8 @@ int tv_verify_attn_path(const tv_attn_args* a);
 
 /* How many kernels one tv_verify_attn call with these arguments enqueues (for launch
  * accounting; the CUDA-core path: attention + split combine; the tensor-core path: work
- * schedule + key gather for a paged cache + attention + split combine), or a negative
- * tv_status if the arguments are invalid. */
+ * preparation + key gather for a large paged cache + attention + split combine), or a
+ * negative tv_status if the arguments are invalid. */
 int tv_verify_attn_launches(const tv_attn_args* a);
 
 /*

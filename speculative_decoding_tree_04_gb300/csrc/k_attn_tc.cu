@@ -33,11 +33,21 @@
 // (thread = tile row, matching TMEM lanes; on rank 0 thread 0 of them also issues the
 // message copies); warps 2-3 idle.
 //
-// Keys come from a row-major view of the cache (c_kv row, k_pe row per key).  A 128-key
-// box needs 128 consecutive rows, so a paged cache (64-key pages in any order) is first
-// gathered into a contiguous copy in the workspace by gather_kv_kernel; a contiguous
-// cache is read in place.  Tiles are handed out round-robin to the persistent clusters;
-// long KV ranges may be split across tiles and merged by the split combine kernel.
+// Keys come from a row-major view (c_kv row, k_pe row per key); a 128-key step of such a
+// view is one box of 128 consecutive rows.  A contiguous cache is that view.  A paged
+// cache keeps 64-key pages in any order and is handled one of two ways:
+//   - large caches: gather_kv_kernel first copies the pages into a contiguous view in the
+//     workspace.  The copy runs at HBM speed and leaves the freshest part in L2, which the
+//     attention kernel's key stream then hits.
+//   - smaller ones (and any whose copy would not fit 32-bit TMA row coordinates): every
+//     128-key step of every sequence gets its own tensor maps, built by prep_kernel -- a
+//     5-D view {64 elements, 8 rows, 8 row groups, 2 pages, chunks} whose page dimension
+//     strides from the step's lower page to its other page, so that one box lands both
+//     pages' rows in the 128-row layout the MMA reads.  If the step's second page lies
+//     below its first, the view starts at the lower one and S comes out with its two
+//     halves swapped, which the softmax undoes.
+// Tiles are handed out longest first to the persistent clusters; long KV ranges may be
+// split across tiles and merged by the split combine kernel.
 //
 // Every wait is bounded (a wall-clock deadline); on expiry the kernel records
 // TV_ERR_TIMEOUT, tells the peer CTA, drains its tensor-core work, frees its TMEM and
@@ -94,8 +104,12 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
 struct TcParams {
   const __nv_bfloat16* q_latent;
   const __nv_bfloat16* q_pe;
-  int64_t seq_rows;  // rows between consecutive sequences in the key view
+  int64_t seq_rows;  // contiguous cache: rows between consecutive sequences
   int64_t seq_cap;   // longest KV a sequence may have
+  const CUtensorMap* step_maps;  // paged cache: [B][steps_per_seq][latent, rope] maps
+  const uint8_t* step_swap;      // paged cache: 1 where a step's pages come in swapped
+  const int32_t* page_table;
+  int32_t steps_per_seq, max_pages, paged;
   const int32_t* prefix_len;
   const uint64_t* anc;
   float* out;
@@ -107,7 +121,6 @@ struct TcParams {
   int32_t B, H, Q, max_prefix;
   int32_t tiles_per_seq, splits, chunk, n_items;
   const int4* info;  // per work item: sequence, split, tile, prefix length (longest first)
-  int32_t wait_all;  // 1: the records come from the kernel just before (wait before any read)
   float scale_log2;
 };
 
@@ -178,8 +191,21 @@ __device__ __forceinline__ int sweep_step(const Item& it, int j) {
   return jj >= it.ns ? jj - it.ns : jj;
 }
 
+// Cache row of key `key` (relative to the item's first key) of a contiguous cache.
 __device__ __forceinline__ int64_t key_row(const TcParams& p, const Item& it, int64_t key) {
   return (int64_t)it.b * p.seq_rows + it.k0 + key;
+}
+
+// Cache row of the first key of 64-key block `blk` (relative to the item's first key).
+__device__ __forceinline__ int64_t block_row(const TcParams& p, const Item& it, int blk) {
+  if (!p.paged) return key_row(p, it, (int64_t)blk * kBN);
+  const int64_t lb = (it.k0 >> 6) + blk;
+  return (int64_t)__ldg(p.page_table + (int64_t)it.b * p.max_pages + lb) * kBN;
+}
+
+// Index of a step's tensor maps / swap flag (paged cache).
+__device__ __forceinline__ int64_t step_index(const TcParams& p, const Item& it, int step) {
+  return (int64_t)it.b * p.steps_per_seq + (it.k0 >> 7) + step;
 }
 
 __device__ __forceinline__ void raise_abort(Shared& sh, int32_t* status, int code) {
@@ -310,24 +336,57 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
   if (warp == 0) {
     // ---------------- TMA producer: four latent boxes and the rope box per step --------
     if (lane == 0) {
-      griddep_wait();  // the key view may still be being written by the gather kernel
       prefetch_tensormap(map_lat);
       prefetch_tensormap(map_kpe);
+      // The refill latency of the rings is on the critical path: each cache layout gets its
+      // own lean loop (the branch is taken once per tile).
       uint32_t u = 0, rc = 0;
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
+        if (!p.paged) {
+          for (int j = 0; j < it.ns; ++j, ++rc) {
+            const int row0 = (int)key_row(p, it, (int64_t)sweep_step(it, j) * kStep);
+            for (int h = 0; h < 4; ++h, ++u) {
+              const uint32_t st = u % kNLS;
+              if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
+              mbar_arrive_expect_tx(&sh.slat_full[st], kStageS);
+              tma_load_3d(lat + st * kStageS, map_lat, 0, row0, 2 * h, &sh.slat_full[st]);
+            }
+            const uint32_t rs = rc % kNRope;
+            if (!wait_bar(sh, &sh.rope_empty[rs], ((rc / kNRope) & 1) ^ 1, p.status)) return;
+            mbar_arrive_expect_tx(&sh.rope_full[rs], kChunkS);
+            tma_load_2d(rope + rs * kChunkS, map_kpe, 0, row0, &sh.rope_full[rs]);
+          }
+          continue;
+        }
+        // paged cache: per-step maps, written by prep_kernel; acquired for the whole tile
+        // up front, each step's prefetched one step ahead
+        const CUtensorMap* mb = p.step_maps + 2 * step_index(p, it, 0);
+        for (int jj = 0; jj < it.ns; ++jj) {
+          tmap_acquire(mb + 2 * jj);
+          tmap_acquire(mb + 2 * jj + 1);
+        }
+        if (it.ns > 0) {
+          prefetch_tensormap(mb + 2 * sweep_step(it, 0));
+          prefetch_tensormap(mb + 2 * sweep_step(it, 0) + 1);
+        }
         for (int j = 0; j < it.ns; ++j, ++rc) {
-          const int row0 = (int)key_row(p, it, (int64_t)sweep_step(it, j) * kStep);
+          const CUtensorMap* ml = mb + 2 * sweep_step(it, j);
+          if (j + 1 < it.ns) {
+            const CUtensorMap* mn = mb + 2 * sweep_step(it, j + 1);
+            prefetch_tensormap(mn);
+            prefetch_tensormap(mn + 1);
+          }
           for (int h = 0; h < 4; ++h, ++u) {
             const uint32_t st = u % kNLS;
             if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
             mbar_arrive_expect_tx(&sh.slat_full[st], kStageS);
-            tma_load_3d(lat + st * kStageS, map_lat, 0, row0, 2 * h, &sh.slat_full[st]);
+            tma_load_5d(lat + st * kStageS, ml, 0, 0, 0, 0, 2 * h, &sh.slat_full[st]);
           }
           const uint32_t rs = rc % kNRope;
           if (!wait_bar(sh, &sh.rope_empty[rs], ((rc / kNRope) & 1) ^ 1, p.status)) return;
           mbar_arrive_expect_tx(&sh.rope_full[rs], kChunkS);
-          tma_load_2d(rope + rs * kChunkS, map_kpe, 0, row0, &sh.rope_full[rs]);
+          tma_load_4d(rope + rs * kChunkS, ml + 1, 0, 0, 0, 0, &sh.rope_full[rs]);
         }
       }
     }
@@ -463,6 +522,8 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       mbar_arrive(&sh.q_ready);
 
       float m = -INFINITY, l = 0.f;
+      uint32_t swap_next =
+          (p.paged && __ldg(p.step_swap + step_index(p, it, sweep_step(it, 0)))) ? 64u : 0u;
       for (int j = 0; j < it.ns; ++j, ++sc) {
         if (j == (it.ns > 3 ? it.ns - 3 : 0) && item_next >= 0) {
           // warm L2 with the next tile's queries a few steps before they are needed (the
@@ -481,6 +542,12 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         const bool okf =
             __all_sync(0xffffffffu, wait_bar(sh, &sh.s_full[sb], (sc >> 1) & 1, p.status));
         float t[128];
+        const int st = sweep_step(it, j);
+        // paged cache: a step whose second page lies below its first holds the second
+        // page's keys in S columns 0..63 (the flag is read a step ahead)
+        const uint32_t sw64 = swap_next;
+        if (p.paged && j + 1 < it.ns)
+          swap_next = __ldg(p.step_swap + step_index(p, it, sweep_step(it, j + 1))) ? 64u : 0u;
         if (!okf) {
 #pragma unroll
           for (int k = 0; k < 128; ++k) t[k] = 0.f;
@@ -488,17 +555,16 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           tc_fence_after();
           uint32_t sr[128];
           const uint32_t ta = tmem + lane_base + (sb ? kTmS1 : kTmS0);
-          tmem_ld32(ta, sr);
-          tmem_ld32(ta + 32, sr + 32);
-          tmem_ld32(ta + 64, sr + 64);
-          tmem_ld32(ta + 96, sr + 96);
+          tmem_ld32(ta + sw64, sr);
+          tmem_ld32(ta + sw64 + 32, sr + 32);
+          tmem_ld32(ta + (sw64 ^ 64u), sr + 64);
+          tmem_ld32(ta + (sw64 ^ 64u) + 32, sr + 96);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(&sh.s_empty[sb]);
 #pragma unroll
           for (int k = 0; k < 128; ++k) t[k] = __uint_as_float(sr[k]);
         }
-        const int st = sweep_step(it, j);
         const bool two = 2 * st + 1 < it.nb;
         const int64_t key0 = it.k0 + (int64_t)st * kStep;
         const uint64_t vis0 =
@@ -592,16 +658,28 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
   if (warp == 0) {
     // ---------------- TMA producer: each 64-key block's latent chunks, in message order --
     if (lane == 0) {
-      griddep_wait();  // the key view may still be being written by the gather kernel
       prefetch_tensormap(map_lat);
       uint32_t u = 0;
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
+        // cache rows of each step's blocks are looked up a step ahead
+        int rows_next[2] = {0, 0};
+        if (it.ns > 0) {
+          const int s0 = sweep_step(it, 0);
+          rows_next[0] = (int)block_row(p, it, 2 * s0);
+          if (2 * s0 + 1 < it.nb) rows_next[1] = (int)block_row(p, it, 2 * s0 + 1);
+        }
         for (int j = 0; j < it.ns; ++j) {
           const int st = sweep_step(it, j);
           const int nh = 2 * st + 1 < it.nb ? 2 : 1;
+          const int rows_cur[2] = {rows_next[0], rows_next[1]};
+          if (j + 1 < it.ns) {
+            const int s1 = sweep_step(it, j + 1);
+            rows_next[0] = (int)block_row(p, it, 2 * s1);
+            if (2 * s1 + 1 < it.nb) rows_next[1] = (int)block_row(p, it, 2 * s1 + 1);
+          }
           for (int hh = 0; hh < nh; ++hh) {
-            const int row0 = (int)key_row(p, it, (int64_t)(2 * st + hh) * kBN);
+            const int row0 = rows_cur[hh];
             for (int h = 0; h < 2; ++h, ++u) {
               const uint32_t ls = u % kNLO;
               if (!wait_bar(sh, &sh.olat_empty[ls], ((u / kNLO) & 1) ^ 1, p.status)) return;
@@ -761,10 +839,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
     return;
   }
   Shared& sh = *reinterpret_cast<Shared*>(smem + kSideMax);
-  // The kernel may start while the kernel before it in the stream still runs (programmatic
-  // dependent launch).  Everything written before that kernel is visible; its own output
-  // (the key view, or the work records when no gather runs) is waited for before use.
-  if (p.wait_all) griddep_wait();
   const uint32_t rank = cluster_rank();
   const int warp = threadIdx.x >> 5;
 
@@ -813,6 +887,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // barriers of both CTAs exist before any remote arrive or store
+  // The kernel may start while prep_kernel (just before it in the stream) still runs
+  // (programmatic dependent launch): the set-up above overlaps it, and everything below
+  // reads its work records and step maps only after this wait.
+  griddep_wait();
 
   if (rank == 0)
     s_side(p, &map_lat_s, &map_kpe_s, sh, smem);
@@ -858,17 +936,69 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
   }
 }
 
-// Orders the (sequence, split) pairs by their number of key blocks, longest first (ties by
-// index), for the snake schedule of the attention kernel, and writes one record per work
-// item.  One CTA ranks all pairs against each other; beyond kMaxRanked pairs the order
-// stays the identity.
+// Work preparation, one launch before the attention kernel.
+//  - Block 0 orders the (sequence, split) pairs by their number of key blocks, longest
+//    first (ties by index), and writes one record per work item (sequence, split, tile,
+//    prefix length) for the snake schedule.  Beyond kMaxRanked pairs the order stays the
+//    identity.
+//  - Paged cache: the other blocks write, for every 128-key step of every sequence, the
+//    step's two tensor maps (latent and rope).  Each is a copy of a host-encoded template
+//    with a new base (the step's lower page), page-dimension stride (distance to its other
+//    page; 0 if both are the same page) and, when the step has one page only, page extent
+//    1 (the missing half reads as zeros).  A page index outside the cache rows is reported
+//    as TV_ERR_BOUNDS and replaced by page 0 (that sequence's result is then undefined, as
+//    for any out-of-range input).
 constexpr int kMaxRanked = 1024;
 __global__ void __launch_bounds__(1024)
-schedule_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, int chunk,
-                int max_prefix, int64_t seq_cap, int tiles, int n_items, int4* __restrict__ info) {
+prep_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, int chunk,
+            int max_prefix, int64_t seq_cap, int tiles, int n_items, int4* __restrict__ info,
+            const __grid_constant__ CUtensorMap tmpl_lat, const __grid_constant__ CUtensorMap tmpl_rope,
+            const unsigned char* ckv, int64_t ckv_page_bytes, const unsigned char* kpe,
+            int64_t kpe_page_bytes, const int32_t* __restrict__ page_table, int max_pages,
+            int64_t num_pages, int steps_per_seq, CUtensorMap* __restrict__ maps,
+            uint8_t* __restrict__ swap, int32_t* status) {
+  griddep_launch_dependents();  // the attention kernel may start its set-up now
+  if (blockIdx.x > 0) {
+    const int64_t idx = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)B * steps_per_seq) return;
+    const int b = (int)(idx / steps_per_seq), sp = (int)(idx - (int64_t)b * steps_per_seq);
+    const int P = prefix_len[b];
+    const int64_t kv = (int64_t)P + Q;
+    if (P < 0 || P > max_prefix || kv > seq_cap) return;  // reported by the attention kernel
+    const int64_t nblk = (kv + kBN - 1) / kBN;
+    if (2 * (int64_t)sp >= nblk) return;  // beyond this sequence: never used
+    int64_t pa = page_table[(int64_t)b * max_pages + 2 * sp];
+    const bool has_b = 2 * (int64_t)sp + 1 < nblk;
+    int64_t pb = has_b ? page_table[(int64_t)b * max_pages + 2 * sp + 1] : pa;
+    if (pa < 0 || pa >= num_pages || pb < 0 || pb >= num_pages) {
+      report(status, TV_ERR_BOUNDS);
+      pa = pb = 0;
+    }
+    const int64_t lo = pa < pb ? pa : pb, dist = pa < pb ? pb - pa : pa - pb;
+    CUtensorMap* m = maps + 2 * idx;
+    const uint4* tl = reinterpret_cast<const uint4*>(&tmpl_lat);
+    const uint4* tr = reinterpret_cast<const uint4*>(&tmpl_rope);
+    uint4* ml = reinterpret_cast<uint4*>(m);
+    uint4* mr = reinterpret_cast<uint4*>(m + 1);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      ml[w] = tl[w];
+      mr[w] = tr[w];
+    }
+    tmap_set_address(m, ckv + lo * ckv_page_bytes);
+    tmap_set_stride2(m, (uint64_t)(dist * ckv_page_bytes));
+    tmap_set_address(m + 1, kpe + lo * kpe_page_bytes);
+    tmap_set_stride2(m + 1, (uint64_t)(dist * kpe_page_bytes));
+    if (!has_b) {
+      tmap_set_dim3(m, 1);
+      tmap_set_dim3(m + 1, 1);
+    }
+    swap[idx] = (uint8_t)(pb < pa ? 1 : 0);
+    tmap_release();
+    return;
+  }
   __shared__ int cost[kMaxRanked];
   __shared__ int order[kMaxRanked];
-  griddep_launch_dependents();  // a following attention kernel waits for these records
   const int n = B * splits;
   const bool ranked = n <= kMaxRanked;
   for (int i = threadIdx.x; ranked && i < n; i += blockDim.x) {
@@ -975,10 +1105,47 @@ int max_clusters() {
   return g_max_clusters[dev];
 }
 
-// Rows per sequence of the gathered key view: the longest KV rounded up to whole steps.
+// Rows per sequence of a gathered key view: the longest KV rounded up to whole steps.
 int64_t gathered_seq_rows(const tv_attn_args* a) {
   const int64_t kv_max = (int64_t)a->max_prefix_len + a->Q;
   return (kv_max + kStep - 1) / kStep * kStep;
+}
+
+// Paged cache: gather it into a contiguous view (true) or use per-step tensor maps (false).
+bool use_gather(const tv_attn_args* a) {
+  if (!a->cache.page_table) return false;
+  const int64_t rows = (int64_t)a->B * gathered_seq_rows(a);
+  return rows < (1ll << 31) && rows * (kDL + kDR) * 2 > (64ll << 20);
+}
+
+// 128-key steps of the longest sequence (per-step tensor maps of a paged cache).
+int64_t steps_per_seq(const tv_attn_args* a) {
+  return ((int64_t)a->max_prefix_len + a->Q + kStep - 1) / kStep;
+}
+
+// Templates of the per-step maps of a paged cache.  Latent: {64 elements, 8 rows, 8 row
+// groups, 2 pages, 8 chunks} with strides {row, 8 rows, page placeholder, 128 bytes}, box
+// {64, 8, 8, 2, 2} (two chunks of 128 keys, the same shared-memory layout as a 3-D box of
+// 128 consecutive rows).  Rope: {64 elements, 8 rows, 8 row groups, 2 pages}, box = all.
+bool make_step_templates(CUtensorMap* lat, CUtensorMap* rope, const tv_attn_args* a) {
+  const uint64_t rb = (uint64_t)a->ckv_row_stride * 2, rbk = (uint64_t)a->kpe_row_stride * 2;
+  {
+    cuuint64_t dims[5] = {64, 8, 8, 2, kDL / 64};
+    cuuint64_t strides[4] = {rb, 8 * rb, 64 * rb, 128};
+    cuuint32_t box[5] = {64, 8, 8, 2, 2};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (g_encode(lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a->c_kv), dims, strides,
+                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  cuuint64_t dims[4] = {kDR, 8, 8, 2};
+  cuuint64_t strides[3] = {rbk, 8 * rbk, 64 * rbk};
+  cuuint32_t box[4] = {64, 8, 8, 2};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return g_encode(rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a->k_pe), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -989,9 +1156,7 @@ bool tc_supported(const tv_attn_args* a) {
   if (!(a->q_dt == TV_BF16 && a->kv_dt == TV_BF16 && a->d_latent == kDL && a->d_rope == kDR &&
         a->cache.num_rows > 0 && a->cache.num_rows < (1ll << 31)))
     return false;
-  if (a->cache.page_table == nullptr) return true;
-  // the gathered copy is addressed with 32-bit TMA row coordinates too
-  return a->cache.page_size == kBN && (int64_t)a->B * gathered_seq_rows(a) < (1ll << 31);
+  return a->cache.page_table == nullptr || a->cache.page_size == kBN;
 }
 
 TcPlan tc_plan(const tv_attn_args* a) {
@@ -1037,16 +1202,24 @@ TcPlan tc_plan(const tv_attn_args* a) {
   return p;
 }
 
-// Workspace: [work-item records][split partial outputs][split partial lse][gathered keys
-// (paged caches)].
+// Workspace: [work-item records][split partial outputs][split partial lse][paged cache:
+// gathered key view, or per-step tensor maps (2 x 128 B per step) and swap flags].
 size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) {
   const size_t rows = (size_t)a->B * a->Q * a->H;
   size_t n = align256((size_t)p.n_items * 16);
   if (p.splits > 1)
     n += align256((size_t)p.splits * rows * a->d_latent * 4) + align256((size_t)p.splits * rows * 4);
-  if (a->cache.page_table)
+  if (use_gather(a)) {
     n += align256((size_t)a->B * (size_t)gathered_seq_rows(a) * (kDL + kDR) * 2);
+  } else if (a->cache.page_table) {
+    const size_t steps = (size_t)a->B * (size_t)steps_per_seq(a);
+    n += align256(steps * 2 * sizeof(CUtensorMap)) + align256(steps);
+  }
   return n;
+}
+
+int tc_launch_count(const tv_attn_args* a, const TcPlan& p) {
+  return 2 + (use_gather(a) ? 1 : 0) + (p.splits > 1 ? 1 : 0);
 }
 
 cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cudaStream_t st) {
@@ -1064,12 +1237,22 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     ws_lse = (float*)wsp;
     wsp += align256((size_t)pl.splits * rows * 4);
   }
-  const bool paged = a->cache.page_table != nullptr;
+  const bool gather = use_gather(a);
+  const bool paged = a->cache.page_table != nullptr && !gather;  // per-step maps
+  const int64_t steps = paged ? steps_per_seq(a) : 0;
+  CUtensorMap* maps = nullptr;
+  uint8_t* swap = nullptr;
+  if (paged) {
+    maps = (CUtensorMap*)wsp;
+    wsp += align256((size_t)a->B * steps * 2 * sizeof(CUtensorMap));
+    swap = (uint8_t*)wsp;
+  }
+  // the key view the attention kernel reads rows of: the cache, or its gathered copy
+  int64_t seq_rows, seq_cap;
+  uint64_t key_rows, lat_row_bytes, kpe_row_bytes;
   const void* lat_base;
   const void* kpe_base;
-  uint64_t lat_row_bytes, kpe_row_bytes, key_rows;
-  int64_t seq_rows, seq_cap;
-  if (paged) {
+  if (gather) {
     seq_rows = gathered_seq_rows(a);
     seq_cap = std::min<int64_t>(seq_rows, (int64_t)a->cache.max_pages * kBN);
     key_rows = (uint64_t)a->B * (uint64_t)seq_rows;
@@ -1077,18 +1260,25 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     kpe_base = wsp + kDL * 2;
     lat_row_bytes = kpe_row_bytes = (kDL + kDR) * 2;
   } else {
-    seq_rows = seq_cap = a->cache.kv_stride_b;
+    seq_rows = paged ? 0 : a->cache.kv_stride_b;
+    seq_cap = paged ? (int64_t)a->cache.max_pages * kBN : a->cache.kv_stride_b;
     key_rows = (uint64_t)a->cache.num_rows;
     lat_base = a->c_kv;
     kpe_base = a->k_pe;
     lat_row_bytes = (uint64_t)a->ckv_row_stride * 2;
     kpe_row_bytes = (uint64_t)a->kpe_row_stride * 2;
   }
-  CUtensorMap m_lat_s, m_kpe_s, m_lat_o;
+  // S-side maps over the row view (unused with per-step maps) and the O-side map
+  CUtensorMap m_lat_s, m_kpe_s, m_lat_o, t_lat, t_rope;
   if (!make_map_latent(&m_lat_s, lat_base, key_rows, lat_row_bytes, kStep, 2) ||
       !make_map_rope(&m_kpe_s, kpe_base, key_rows, kpe_row_bytes, kStep) ||
       !make_map_latent(&m_lat_o, lat_base, key_rows, lat_row_bytes, kBN, 4))
     return cudaErrorInvalidValue;
+  if (paged && !make_step_templates(&t_lat, &t_rope, a)) return cudaErrorInvalidValue;
+  if (!paged) {
+    t_lat = m_lat_s;  // not used
+    t_rope = m_kpe_s;
+  }
 
   TcParams p{};
   p.q_latent = (const __nv_bfloat16*)a->q_latent;
@@ -1112,14 +1302,27 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.chunk = pl.chunk;
   p.n_items = pl.n_items;
   p.info = info;
-  p.wait_all = paged ? 0 : 1;
+  p.step_maps = maps;
+  p.step_swap = swap;
+  p.page_table = a->cache.page_table;
+  p.steps_per_seq = (int32_t)steps;
+  p.max_pages = a->cache.max_pages;
+  p.paged = paged ? 1 : 0;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
   if (p.n_items == 0) return cudaSuccess;
 
-  schedule_kernel<<<1, 1024, 0, st>>>(a->prefix_len, a->B, a->Q, pl.splits, pl.chunk,
-                                      a->max_prefix_len, seq_cap, pl.tiles_per_seq, pl.n_items,
-                                      info);
-  if (paged) {
+  {
+    const int64_t map_blocks = paged ? (a->B * steps + 1023) / 1024 : 0;
+    prep_kernel<<<(unsigned)(1 + map_blocks), 1024, 0, st>>>(
+        a->prefix_len, a->B, a->Q, pl.splits, pl.chunk, a->max_prefix_len, seq_cap,
+        pl.tiles_per_seq, pl.n_items, info, t_lat, t_rope, (const unsigned char*)a->c_kv,
+        (int64_t)lat_row_bytes * kBN, (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN,
+        a->cache.page_table, a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps, maps,
+        swap, a->status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (gather) {
     const dim3 grid((unsigned)(seq_rows / kBN), (unsigned)a->B);
     gather_kv_kernel<<<grid, 256, 0, st>>>(
         (const uint4*)a->c_kv, a->ckv_row_stride / 8, (const uint4*)a->k_pe, a->kpe_row_stride / 8,

@@ -45,6 +45,33 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ---- tensor maps edited on the device ------------------------------------------------
+// A copy of a host-encoded map in global memory gets a new base address, a new byte stride
+// for dimension dim+1 (`dim` indexes the stride array), or a new extent for dimension dim.
+__device__ __forceinline__ void tmap_set_address(void* map, const void* addr) {
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(map),
+               "l"((uint64_t)addr)
+               : "memory");
+}
+__device__ __forceinline__ void tmap_set_stride2(void* map, uint64_t stride_bytes) {
+  asm volatile("tensormap.replace.tile.global_stride.global.b1024.b64 [%0], 2, %1;" ::"l"(map),
+               "l"(stride_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tmap_set_dim3(void* map, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 3, %1;" ::"l"(map),
+               "r"(extent)
+               : "memory");
+}
+// Writer side: order this thread's edits before later uses of the maps by the TMA engine.
+__device__ __forceinline__ void tmap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+// Reader side, before a TMA load through a map edited by another kernel.
+__device__ __forceinline__ void tmap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
 // ---- programmatic dependent launch ----------------------------------------------------
 // Wait until the grid this one depends on (the previous kernel in the stream, when this one
 // was launched with programmatic stream serialisation) has finished and its memory is
@@ -116,6 +143,22 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, int c4, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
 // 3-D tile load delivered to every CTA of the cluster named in `mask`, at the same shared
 // offset in each, signalling the mbarrier at the same offset in each.
 __device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorMap* map, int c0,
@@ -126,6 +169,20 @@ __device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorM
       ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
+}
+// Ask the TMA engine to bring a box into L2 without delivering it to shared memory.
+__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                   int c3, int c4) {
+  asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                   map),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                   int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

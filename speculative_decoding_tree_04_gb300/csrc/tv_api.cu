@@ -176,10 +176,7 @@ int tv_verify_attn_path(const tv_attn_args* a) {
 int tv_verify_attn_launches(const tv_attn_args* a) {
   const int path = tv_verify_attn_path(a);
   if (path < 0) return path;
-  if (path == TV_PATH_TCGEN05) {
-    const tv::TcPlan p = tv::tc_plan(a);
-    return 2 + (a->cache.page_table ? 1 : 0) + (p.splits > 1 ? 1 : 0);
-  }
+  if (path == TV_PATH_TCGEN05) return tv::tc_launch_count(a, tv::tc_plan(a));
   return 1 + (tv::simt_plan(a, sm_count()).splits > 1 ? 1 : 0);
 }
 

@@ -65,6 +65,7 @@ bool tc_supported(const tv_attn_args* a);
 TcPlan tc_plan(const tv_attn_args* a);
 size_t tc_workspace(const tv_attn_args* a, const TcPlan& p);
 cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& p, void* ws, cudaStream_t st);
+int tc_launch_count(const tv_attn_args* a, const TcPlan& p);  // kernels launch_attn_tc enqueues
 
 // Split-KV combine: partial (out_s, lse_s) for s < splits -> final out, lse.
 cudaError_t launch_combine(const float* ws_out, const float* ws_lse, int splits,

@@ -134,6 +134,22 @@ def test_edge_cases_tensor_cores(desc, kw, splits):
     check_step(inp, g, o)
 
 
+def test_tc_paged_repeated_and_reversed_pages():
+    """Paged cache, tensor cores, per-step tensor maps: two logical blocks of one sequence on
+    the same physical page (the map's page stride is then zero) and a step whose second page
+    lies below its first (the S halves come out swapped).  The oracle reads the same page
+    table."""
+    inp = synth.generate(seed=77, dtype="bf16", B=2, H=16, Q=5, DL=512, DR=64,
+                         prefix=(300, 400), paged=True)
+    pt = inp["page_table"].copy()
+    pt[0, 1] = pt[0, 0]
+    a, b = int(pt[1, 2]), int(pt[1, 3])
+    pt[1, 2], pt[1, 3] = max(a, b), min(a, b)
+    inp["page_table"] = pt
+    step, g, o = run_pair(inp, path=tv.PATH_TCGEN05)
+    check_step(inp, g, o)
+
+
 def test_sharp_softmax_simt():
     inp = synth.generate(seed=5, dtype="fp32", B=2, H=16, Q=9, DL=512, DR=64,
                          prefix=(300, 900), q_var=0.02)

@@ -129,7 +129,7 @@ struct Shared {
   uint64_t olat_full[kNLO], olat_empty[kNLO];
   uint64_t rope_full[kNRope], rope_empty[kNRope];
   uint64_t s_full[2], s_empty[2];
-  uint64_t q_ready, q_free, pdst_free[kNInbox];
+  uint64_t qr_full, q_free, pdst_free[kNInbox];
   uint64_t p_full[kNInbox];
   uint64_t drain, job_full, corr_done, epi_done, final_bar;
   uint32_t tmem_base;
@@ -294,23 +294,6 @@ __device__ __forceinline__ float emit_half(const float* t, float c, float mr, un
   return (a0 + a1) + (b0 + b1);
 }
 
-// Two 32-column chunks of a row's latent queries (16 x 16 bytes) into TMEM at `taddr`.
-__device__ __forceinline__ void store_q_chunks(uint32_t taddr, const uint4* v) {
-  uint32_t w[2][32];
-#pragma unroll
-  for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      w[cc][4 * e + 0] = v[8 * cc + e].x;
-      w[cc][4 * e + 1] = v[8 * cc + e].y;
-      w[cc][4 * e + 2] = v[8 * cc + e].z;
-      w[cc][4 * e + 3] = v[8 * cc + e].w;
-    }
-  __syncwarp();
-  tmem_st32(taddr, w[0]);
-  tmem_st32(taddr + 32, w[1]);
-}
-
 // Masked keys of a 64-key half get score -inf.
 __device__ __forceinline__ void apply_mask(float* t, uint64_t vis) {
   if (vis == ~0ull) return;
@@ -325,7 +308,8 @@ __device__ __forceinline__ void apply_mask(float* t, uint64_t vis) {
 // rank 0: QK^T + softmax
 // ===================================================================================
 __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUtensorMap* map_kpe,
-                       Shared& sh, unsigned char* smem) {
+                       const CUtensorMap* map_q, const CUtensorMap* map_qr, Shared& sh,
+                       unsigned char* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* lat = smem;
   unsigned char* rope = smem + kRopeOff;
@@ -335,14 +319,31 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
 
   if (warp == 0) {
     // ---------------- TMA producer: four latent boxes and the rope box per step --------
+    // Each tile starts with its latent queries, which pass through the key ring (the same
+    // four box shapes) on their way into TMEM, and its rope queries, which go straight to
+    // their buffer once the previous tile's MMAs are done with it.
     if (lane == 0) {
       prefetch_tensormap(map_lat);
       prefetch_tensormap(map_kpe);
+      prefetch_tensormap(map_q);
+      prefetch_tensormap(map_qr);
       // The refill latency of the rings is on the critical path: each cache layout gets its
       // own lean loop (the branch is taken once per tile).
-      uint32_t u = 0, rc = 0;
+      uint32_t u = 0, rc = 0, qi = 0;
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
+        if (it.ns == 0) continue;
+        const int qrow0 = it.b * p.Q * p.H + it.t * kRows;
+        for (int h = 0; h < 4; ++h, ++u) {
+          const uint32_t st = u % kNLS;
+          if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&sh.slat_full[st], kStageS);
+          tma_load_3d(lat + st * kStageS, map_q, 0, qrow0, 2 * h, &sh.slat_full[st]);
+        }
+        if (!wait_bar_cta(sh, &sh.q_free, (qi & 1) ^ 1, p.status)) return;
+        ++qi;
+        mbar_arrive_expect_tx(&sh.qr_full, kChunkS);
+        tma_load_2d(qrope, map_qr, 0, qrow0, &sh.qr_full);
         if (!p.paged) {
           for (int j = 0; j < it.ns; ++j, ++rc) {
             const int row0 = (int)key_row(p, it, (int64_t)sweep_step(it, j) * kStep);
@@ -405,9 +406,29 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         if (it.ns == 0) continue;
-        if (!wait_bar(sh, &sh.q_ready, qc & 1, p.status)) break;
-        ++qc;
+        // The tile's latent queries arrive through the key ring as four stages; they are
+        // copied into TMEM once the previous tile's MMAs have finished reading it.
+        if (!wait_bar_cta(sh, &sh.q_free, (qc & 1) ^ 1, p.status)) break;
         tc_fence_after();
+        bool okq = true;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          if (!wait_bar_cta(sh, &sh.slat_full[st], sph, p.status)) { okq = false; break; }
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tmem_cp_128x256b(tmem + kTmQ + 32 * (2 * h + c) + 8 * kk,
+                               db + (uint64_t)((c * kChunkS + 32 * kk) >> 4));
+          mma_commit(&sh.slat_empty[st]);
+          db += kStageS >> 4;
+          if (++st == kNLS) {
+            st = 0;
+            sph ^= 1;
+            db = dl0;
+          }
+        }
+        if (!okq || !wait_bar_cta(sh, &sh.qr_full, qc & 1, p.status)) break;
         for (int j = 0; j < it.ns && !sh.abort; ++j, ++sc, ++rc) {
           const uint32_t sb = sc & 1;
           if (!wait_bar_cta(sh, &sh.s_empty[sb], ((sc >> 1) & 1) ^ 1, p.status)) break;
@@ -440,6 +461,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           mma_commit(&sh.s_full[sb]);
         }
         mma_commit(&sh.q_free);
+        ++qc;
       }
       mma_commit(&sh.final_bar);
       wait_bar(sh, &sh.final_bar, 0, p.status);
@@ -460,10 +482,10 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     // The four warps leave their loops only together, at a 128-thread barrier that agrees
     // on the outcome of the waits before it (a warp that left alone would strand the
     // others at the next barrier).
-    uint32_t sc = 0, qc = 0, mc = 0;
+    uint32_t sc = 0, mc = 0;
     bool live = true;
-    // The next item's record is requested a whole tile ahead, so that at a tile boundary
-    // only the query loads stand between the last step and the next tile's first MMAs.
+    // The next item's record is requested a whole tile ahead (its queries reach TMEM
+    // without these warps).
     int item_next = item_at(p, 0, cid, ncl);
     int4 info_next = item_next >= 0 ? item_info(p, item_next) : make_int4(0, 0, 0, 0);
     for (int rr = 0; item_next >= 0 && live; ++rr) {
@@ -483,43 +505,6 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       const int64_t kv_end = (int64_t)it.P + p.Q;
       const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
 
-      // ---- latent queries into TMEM columns [0, 256), rope queries into shared memory ----
-      // The loads are software-pipelined two chunks (32 columns each) at a time, and the
-      // first four chunks and the rope part are requested before waiting for the previous
-      // tile's MMAs to release the query storage.
-      {
-        const uint4* ql = reinterpret_cast<const uint4*>(p.q_latent + grow * kDL);
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q_pe + grow * kDR);
-        uint4 qa[16], qb[16], qp[8];
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) qa[e] = vrow ? __ldg(ql + e) : z;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) qb[e] = vrow ? __ldg(ql + 16 + e) : z;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qp[e] = vrow ? __ldg(qr + e) : z;
-        if (!named_sync_and(3, 128, wait_bar(sh, &sh.q_free, (qc & 1) ^ 1, p.status))) {
-          live = false;
-          break;
-        }
-        ++qc;
-        tc_fence_after();
-        store_q_chunks(tmem + lane_base + kTmQ, qa);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) qa[e] = vrow ? __ldg(ql + 32 + e) : z;
-        store_q_chunks(tmem + lane_base + kTmQ + 64, qb);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) qb[e] = vrow ? __ldg(ql + 48 + e) : z;
-        unsigned char* qrow = qrope + row_off;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) *reinterpret_cast<uint4*>(qrow + (((uint32_t)e ^ sw) << 4)) = qp[e];
-        store_q_chunks(tmem + lane_base + kTmQ + 128, qa);
-        store_q_chunks(tmem + lane_base + kTmQ + 192, qb);
-      }
-      tmem_wait_st();
-      fence_proxy_async_smem();  // the rope queries are read by the MMAs
-      tc_fence_before();
-      mbar_arrive(&sh.q_ready);
 
       float m = -INFINITY, l = 0.f;
       uint32_t swap_next =
@@ -832,7 +817,9 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
                const __grid_constant__ CUtensorMap map_kpe_s,
-               const __grid_constant__ CUtensorMap map_lat_o) {
+               const __grid_constant__ CUtensorMap map_lat_o,
+               const __grid_constant__ CUtensorMap map_q,
+               const __grid_constant__ CUtensorMap map_qr) {
   extern __shared__ __align__(1024) unsigned char smem[];
   if (smem_u32(smem) & 1023u) {  // both CTAs see the same layout, so both leave here
     if (threadIdx.x == 0) report(p.status, TV_ERR_UNSUPPORTED);
@@ -863,7 +850,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
       mbar_init(&sh.pdst_free[i], 1);
       mbar_init(&sh.p_full[i], 1);
     }
-    mbar_init(&sh.q_ready, 128);
+    mbar_init(&sh.qr_full, 1);
     mbar_init(&sh.q_free, 1);
     mbar_init(&sh.drain, 1);
     mbar_init(&sh.job_full, 1);
@@ -893,7 +880,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
   griddep_wait();
 
   if (rank == 0)
-    s_side(p, &map_lat_s, &map_kpe_s, sh, smem);
+    s_side(p, &map_lat_s, &map_kpe_s, &map_q, &map_qr, sh, smem);
   else
     o_side(p, &map_lat_o, sh, smem);
 
@@ -1275,6 +1262,12 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
       !make_map_latent(&m_lat_o, lat_base, key_rows, lat_row_bytes, kBN, 4))
     return cudaErrorInvalidValue;
   if (paged && !make_step_templates(&t_lat, &t_rope, a)) return cudaErrorInvalidValue;
+  // query tiles: 128 rows of latent queries as four {64, 128, 2} boxes, rope queries as one
+  // {64, 128} box (rows past the last one read zeros)
+  CUtensorMap m_q, m_qr;
+  if (!make_map_latent(&m_q, a->q_latent, (uint64_t)rows, kDL * 2, kRows, 2) ||
+      !make_map_rope(&m_qr, a->q_pe, (uint64_t)rows, kDR * 2, kRows))
+    return cudaErrorInvalidValue;
   if (!paged) {
     t_lat = m_lat_s;  // not used
     t_rope = m_kpe_s;
@@ -1347,7 +1340,8 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o);
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o, m_q, m_qr);
   if (e != cudaSuccess || pl.splits == 1) return e;
   return launch_combine(p.ws_out, p.ws_lse, pl.splits, (int64_t)rows, a->d_latent, a->out,
                         a->lse, st);

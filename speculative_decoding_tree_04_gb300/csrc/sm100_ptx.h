@@ -355,6 +355,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 // Completion of this thread's earlier tensor-core ops arrives on the barrier at the same
 // shared-memory offset in every CTA of the cluster whose bit is set in cta_mask.
+// Asynchronous copy of a 128-row x 256-bit matrix from shared memory (described by `sdesc`,
+// as an MMA operand) into TMEM lanes 0..127, 8 columns from `taddr`.  A later tcgen05.mma of
+// the same thread sees the copied data; its completion is tracked by tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "

@@ -5,53 +5,73 @@
 // Decision" (angle and trigonometry in double, converted to float32 at the end),
 // §"The Thinking Process" (cos/sin computed once and reused).
 //
-// One block per (sequence, tree node) row.  The block first computes cos/sin of the
-// node's angles for the d_rope/2 frequencies in double and keeps them in shared memory;
-// every head of that row (all H query heads share the node's position) then reuses them.
-// The rotation is done in double with explicit round-to-nearest multiplies and adds (no
-// contraction), then rounded once to float32 (and once more to bf16 for bf16 storage).
-// GB300's float64 rate is low, so the trigonometry is kept to d_rope/2 calls per row;
-// the per-element work is four double multiplies and two adds.
+// One block per (sequence, tree node) row and group of heads.  The block first computes
+// cos/sin of the node's angles for the d_rope/2 frequencies in double (the frequencies
+// themselves come from the host, where they are computed with the same libm pow the
+// float64 reference uses) and keeps them in shared memory; every head of the group (all
+// H query heads share the node's position) then reuses them.
+//
+// GB300's float64 pipe retires about two operations per clock per SM, so the rotation is
+// not done in double.  Each of cos and sin is split into two floats (hi + lo, 48 bits
+// together); x0*c - x1*s is then formed from exact fp32 products (fma gives each product's
+// rounding error), an exact difference (TwoSum) and the small cross terms, which leaves an
+// error below 2^-44 of |x0*c| + |x1*s| before the one rounding to float32.  Where the
+// result is smaller than 2^-19 of that sum (heavy cancellation, where this bound would not
+// be below a quarter ulp), the element is recomputed in double.  Either way the float32
+// value is within one ulp of the float64 formula rounded once.
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
 
 #include "tv_internal.h"
 
 namespace tv {
 namespace {
 
-template <typename T>
-__device__ __forceinline__ double load_as_double(const T* p);
-template <>
-__device__ __forceinline__ double load_as_double<float>(const float* p) {
-  return (double)*p;
-}
-template <>
-__device__ __forceinline__ double load_as_double<__nv_bfloat16>(const __nv_bfloat16* p) {
-  return (double)__bfloat162float(*p);
-}
-
-template <typename T>
-__device__ __forceinline__ void store_from_double(T* p, double v);
-template <>
-__device__ __forceinline__ void store_from_double<float>(float* p, double v) {
-  *p = __double2float_rn(v);
-}
-template <>
-__device__ __forceinline__ void store_from_double<__nv_bfloat16>(__nv_bfloat16* p, double v) {
-  *p = __float2bfloat16_rn(__double2float_rn(v));
+__device__ __forceinline__ float to_float(float v) { return v; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void store_float(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_float(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
 }
 
 constexpr int kMaxHalf = 256;  // d_rope <= 512
+
+// cos and sin of one angle: in double, and each split into float hi + lo
+struct CosSin {
+  double c, s;
+  float ch, cl, sh, sl;
+};
+
+// float32 rounding of a*C - b*S, where C ~ ch + cl ~ cd and S ~ sh + sl ~ sd (see above)
+__device__ __forceinline__ float rot_out(float a, float b, const CosSin& t) {
+  const float p = __fmul_rn(a, t.ch), ep = __fmaf_rn(a, t.ch, -p);
+  const float q = __fmul_rn(b, t.sh), eq = __fmaf_rn(b, t.sh, -q);
+  const float d = __fsub_rn(p, q);
+  const float bb = __fsub_rn(d, p);  // TwoSum(p, -q): p - q = d + ed exactly
+  const float ed = __fadd_rn(__fsub_rn(p, __fsub_rn(d, bb)), __fsub_rn(-q, bb));
+  const float cross = __fmaf_rn(a, t.cl, -__fmul_rn(b, t.sl));
+  const float tail = __fadd_rn(__fadd_rn(ed, __fsub_rn(ep, eq)), cross);
+  const float y = __fadd_rn(d, tail);
+  if (fabsf(y) >= 0x1p-19f * __fadd_rn(fabsf(p), fabsf(q))) return y;
+  return __double2float_rn(__fma_rn((double)a, t.c, -__dmul_rn((double)b, t.s)));
+}
+
+// inverse frequencies 1 / base^(2k / d_rope), k < d_rope / 2
+struct InvFreq {
+  double v[kMaxHalf];
+};
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(128) rope_kernel(const Tin* in, int64_t isr, int64_t ish,
                                                    Tout* out, int64_t osr, int64_t osh,
                                                    CacheGeom cache, int use_cache, int Q,
-                                                   int NH, int D,
+                                                   int NH, int D, int heads_per_block,
                                                    const int32_t* __restrict__ prefix_len,
                                                    const int32_t* __restrict__ depth,
-                                                   double base) {
-  __shared__ double cs[kMaxHalf][2];
+                                                   const __grid_constant__ InvFreq inv) {
+  __shared__ CosSin cs[kMaxHalf];
   const int64_t r = blockIdx.x;  // b*Q + i
   const int b = (int)(r / Q);
   const int i = (int)(r % Q);
@@ -61,11 +81,13 @@ __global__ void __launch_bounds__(128) rope_kernel(const Tin* in, int64_t isr, i
   const int half = D / 2;
   const double pos = (double)P + (double)dep;
   for (int k = threadIdx.x; k < half; k += blockDim.x) {
-    const double inv = 1.0 / pow(base, (2.0 * (double)k) / (double)D);
-    double s, c;
-    sincos(__dmul_rn(pos, inv), &s, &c);
-    cs[k][0] = c;
-    cs[k][1] = s;
+    CosSin t;
+    sincos(__dmul_rn(pos, inv.v[k]), &t.s, &t.c);
+    t.ch = __double2float_rn(t.c);
+    t.cl = __double2float_rn(__dsub_rn(t.c, (double)t.ch));
+    t.sh = __double2float_rn(t.s);
+    t.sl = __double2float_rn(__dsub_rn(t.s, (double)t.sh));
+    cs[k] = t;
   }
   __syncthreads();
   int64_t orow = r;
@@ -81,18 +103,18 @@ __global__ void __launch_bounds__(128) rope_kernel(const Tin* in, int64_t isr, i
     }
     orow = cache_row(cache, b, j);
   }
-  const Tin* src = in + r * isr;
-  Tout* dst = out + orow * osr;
-  for (int idx = threadIdx.x; idx < NH * half; idx += blockDim.x) {
+  const int h0 = (int)blockIdx.y * heads_per_block;
+  const int nh = min(heads_per_block, NH - h0);
+  const Tin* src = in + r * isr + (int64_t)h0 * ish;
+  Tout* dst = out + orow * osr + (int64_t)h0 * osh;
+  for (int idx = threadIdx.x; idx < nh * half; idx += blockDim.x) {
     const int h = idx / half;
     const int k = idx - h * half;
-    const double x0 = load_as_double(src + h * ish + k);
-    const double x1 = load_as_double(src + h * ish + k + half);
-    const double c = cs[k][0], s = cs[k][1];
-    const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
-    const double y1 = __dadd_rn(__dmul_rn(x1, c), __dmul_rn(x0, s));
-    store_from_double(dst + h * osh + k, y0);
-    store_from_double(dst + h * osh + k + half, y1);
+    const float x0 = to_float(src[h * ish + k]);
+    const float x1 = to_float(src[h * ish + k + half]);
+    const CosSin t = cs[k];
+    store_float(dst + h * osh + k, rot_out(x0, x1, t));         // x0 cos - x1 sin
+    store_float(dst + h * osh + k + half, rot_out(x1, -x0, t));  // x1 cos + x0 sin
   }
 }
 
@@ -105,9 +127,26 @@ cudaError_t launch_t(const void* in, int64_t isr, int64_t ish, void* out, int64_
   if (cache) g = *cache;
   const int64_t rows = (int64_t)B * Q;
   if (rows == 0) return cudaSuccess;
-  rope_kernel<Tin, Tout><<<(unsigned)rows, 128, 0, st>>>(
-      (const Tin*)in, isr, ish, (Tout*)out, osr, osh, g, cache ? 1 : 0, Q, NH, D, prefix_len,
-      depth, base);
+  // the table of the last (base, d_rope) a thread used is kept
+  thread_local InvFreq inv{};
+  thread_local double inv_base = 0.0;
+  thread_local int inv_d = 0;
+  if (inv_base != base || inv_d != D) {
+    for (int k = 0; k < D / 2; ++k)
+      inv.v[k] = 1.0 / std::pow(base, (2.0 * (double)k) / (double)D);
+    inv_base = base;
+    inv_d = D;
+  }
+  // few rows: split each row's heads over several blocks, so that about two blocks per SM
+  // share the work
+  const int64_t want = 2 * (int64_t)current_sm_count();
+  int groups = rows >= want ? 1 : (int)std::min<int64_t>(NH, (want + rows - 1) / rows);
+  if (groups < 1) groups = 1;
+  const int hpb = (NH + groups - 1) / groups;
+  groups = (NH + hpb - 1) / hpb;
+  rope_kernel<Tin, Tout><<<dim3((unsigned)rows, (unsigned)groups), 128, 0, st>>>(
+      (const Tin*)in, isr, ish, (Tout*)out, osr, osh, g, cache ? 1 : 0, Q, NH, D, hpb,
+      prefix_len, depth, inv);
   return cudaGetLastError();
 }
 

@@ -216,6 +216,8 @@ def main():
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tcgen05")
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the plain calls instead of replaying CUDA graphs of them")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller profiler captures)")
@@ -259,8 +261,16 @@ def main():
             pg.barrier()
         torch.cuda.synchronize(dev)
 
+    # The timed steps replay two CUDA graphs of the step's calls (captured once; the same
+    # kernels and arguments as the plain calls, without the host's per-call work), unless
+    # --eager asks for the plain calls.
+    graphs = None if args.eager else step.capture_graphs()
     for _ in range(args.warmup):
-        step.run()
+        if graphs is None:
+            step.run()
+        else:
+            graphs[0].replay()
+            graphs[1].replay()
     barrier()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -275,11 +285,17 @@ def main():
         flush.add_(1.0)                     # cold L2 for every step (outside the events)
         s0, a0, a1, s1 = ev[k]
         s0.record(stream)
-        step.visibility()
-        step.rope_q()
-        step.rope_k()
+        if graphs is None:
+            step.visibility()
+            step.rope_q()
+            step.rope_k()
+        else:
+            graphs[0].replay()
         a0.record(stream)
-        step.attention()
+        if graphs is None:
+            step.attention()
+        else:
+            graphs[1].replay()
         a1.record(stream)
         s1.record(stream)
     barrier()
@@ -298,6 +314,7 @@ def main():
         if rank == 0:
             print(json.dumps({"quick": True, "workload": args.workload, "ms_per_step": ms,
                               "attn_ms": ams, "attn_tflops": flops / (ams * 1e-3) / 1e12,
+                              "launch": "eager" if graphs is None else "graphs",
                               "path": ["auto", "simt", "tcgen05"][path]}), flush=True)
         if pg is not None:
             pg.destroy_process_group()
@@ -389,6 +406,9 @@ def main():
                    if args.workload == "cfg5_bf16" else f"mean {float(inp['prefix_len'].mean()):.0f}",
                    "paged": inp["page_table"] is not None, "path": ["auto", "simt", "tcgen05"][path],
                    "l2": "256 MB buffer written between steps (cold L2); per-step CUDA events",
+                   "launch": "eager calls" if graphs is None else
+                   "CUDA graphs of the calls (visibility+RoPE, attention), captured once",
+                   "e2e_launch": "eager calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_gbs": attn_gbs,
         "attn_ms": ams,

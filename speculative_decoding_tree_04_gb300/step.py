@@ -103,6 +103,28 @@ class VerifyStep:
         self.rope_k(stream)
         self.attention(stream)
 
+    def capture_graphs(self):
+        """Capture the step as two CUDA graphs: (visibility, both RoPE calls) and the
+        attention call.  Replaying them launches the same kernels with the same arguments as
+        ``run()`` without the host's per-call work.  The calls run once eagerly first, so
+        that the library's one-time set-up (occupancy query, driver entry points) happens
+        outside the capture.  The graphs keep this step's buffers and sizes."""
+        cur = torch.cuda.current_stream(self.device)
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            self.run()
+        cur.wait_stream(side)
+        torch.cuda.synchronize(self.device)
+        g_pre, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_pre):
+            self.visibility()
+            self.rope_q()
+            self.rope_k()
+        with torch.cuda.graph(g_attn):
+            self.attention()
+        return g_pre, g_attn
+
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues: visibility, 2 RoPE, and the attention call's own."""
         return 3 + tv.attn_launches(self.attn_args())

@@ -242,3 +242,24 @@ def test_all_six_node_trees_bit_exact():
     vis, dep, ancs = oracle.visibility(par)
     assert np.array_equal(anc.cpu().numpy().view(np.uint64), ancs)
     assert np.array_equal(depth.cpu().numpy(), dep)
+
+
+@pytest.mark.parametrize("name", ["cfg3_bf16", "cfg4_bf16"])
+def test_graph_replay_matches_plain_calls(name):
+    """CUDA-graph replay of the step's calls (as the bench times them) gives the plain calls'
+    results bit for bit, and both match the oracle."""
+    inp = synth.generate(name)
+    step = VerifyStep(inp)
+    step.run()
+    ref = step.results()
+    check_step(inp, ref, oracle.tree_verify_step(inp))
+    g_pre, g_attn = step.capture_graphs()
+    for t in (step.out, step.lse, step.q_pe, step.anc, step.depth):
+        t.zero_()
+    for _ in range(2):
+        g_pre.replay()
+        g_attn.replay()
+    got = step.results()
+    assert got["status"] == 0
+    for k in ("anc", "depth", "q_pe_rot", "k_pe_cache", "out", "lse"):
+        assert np.array_equal(got[k], ref[k]), k

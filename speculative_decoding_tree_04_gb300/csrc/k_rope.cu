@@ -44,7 +44,13 @@ struct CosSin {
   float ch, cl, sh, sl;
 };
 
-// float32 rounding of a*C - b*S, where C ~ ch + cl ~ cd and S ~ sh + sl ~ sd (see above)
+// The double-precision recomputation, kept out of line: inlined, the compiler evaluates it
+// unconditionally (predication), which puts five float64-pipe operations on every element.
+__device__ __noinline__ float rot_out_double(float a, float b, double c, double s) {
+  return __double2float_rn(__fma_rn((double)a, c, -__dmul_rn((double)b, s)));
+}
+
+// float32 rounding of a*C - b*S, where C ~ ch + cl ~ c and S ~ sh + sl ~ s (see above)
 __device__ __forceinline__ float rot_out(float a, float b, const CosSin& t) {
   const float p = __fmul_rn(a, t.ch), ep = __fmaf_rn(a, t.ch, -p);
   const float q = __fmul_rn(b, t.sh), eq = __fmaf_rn(b, t.sh, -q);
@@ -55,7 +61,7 @@ __device__ __forceinline__ float rot_out(float a, float b, const CosSin& t) {
   const float tail = __fadd_rn(__fadd_rn(ed, __fsub_rn(ep, eq)), cross);
   const float y = __fadd_rn(d, tail);
   if (fabsf(y) >= 0x1p-19f * __fadd_rn(fabsf(p), fabsf(q))) return y;
-  return __double2float_rn(__fma_rn((double)a, t.c, -__dmul_rn((double)b, t.s)));
+  return rot_out_double(a, b, t.c, t.s);
 }
 
 // inverse frequencies 1 / base^(2k / d_rope), k < d_rope / 2

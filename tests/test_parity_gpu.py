@@ -263,3 +263,44 @@ def test_graph_replay_matches_plain_calls(name):
     assert got["status"] == 0
     for k in ("anc", "depth", "q_pe_rot", "k_pe_cache", "out", "lse"):
         assert np.array_equal(got[k], ref[k]), k
+
+
+@pytest.mark.parametrize("out_dtype", ["fp32", "bf16"])
+def test_rope_cancelling_inputs(out_dtype):
+    """RoPE on inputs built so that x0*cos - x1*sin (or x1*cos + x0*sin) nearly cancels, or
+    sits near 2^-17 .. 2^-21 of |x0*cos| + |x1*sin|: the outputs must still be the float64
+    formula rounded once.  Besides one unit in the last place, the bound allows 2^-50 of
+    the pair's magnitude, because the device's and libm's double cos/sin may differ in
+    their last bit.  Without the exact fallback the error near cancellation is ~2^-44 of
+    the magnitude, far above this bound."""
+    rng = np.random.default_rng(77)
+    B, Q, H, D = 2, 8, 64, 64
+    half = D // 2
+    P = rng.integers(0, 9000, B).astype(np.int32)
+    depth = rng.integers(0, 8, (B, Q)).astype(np.int32)
+    pos = (P[:, None] + depth).astype(np.float64)[:, :, None, None]
+    inv = 1.0 / np.power(10000.0, 2.0 * np.arange(half) / D)
+    c, s = np.cos(pos * inv), np.sin(pos * inv)
+    x0 = rng.standard_normal((B, Q, H, half)).astype(np.float32)
+    x1 = rng.standard_normal((B, Q, H, half)).astype(np.float32)
+    x064 = x0.astype(np.float64)
+    mode = np.arange(H)[None, None, :, None] % 4
+    ok_s, ok_c = np.abs(s) > 1e-3, np.abs(c) > 1e-3
+    a = np.where(ok_s, x064 * c / np.where(ok_s, s, 1.0), x1).astype(np.float32)  # y0 ~ 0
+    b = np.where(ok_c, -x064 * s / np.where(ok_c, c, 1.0), x1).astype(np.float32)  # y1 ~ 0
+    f = np.exp2(-rng.choice([17.0, 19.0, 21.0], x0.shape))
+    t = np.where(ok_s, (x064 * c - f * np.abs(x064 * c)) / np.where(ok_s, s, 1.0), x1)
+    x1 = np.where(mode == 0, a, np.where(mode == 1, b, np.where(mode == 2, t.astype(np.float32), x1)))
+    x1 = (x1.view(np.int32) + rng.integers(-3, 4, x1.shape).astype(np.int32)).view(np.float32)
+    x = np.concatenate([x0, x1], axis=-1).astype(np.float32)
+
+    dev = torch.device("cuda")
+    xt = torch.from_numpy(x).to(dev)
+    out = torch.empty(x.shape, dtype=torch.float32 if out_dtype == "fp32" else torch.bfloat16,
+                      device=dev)
+    tv.rope_neox(xt, out, torch.from_numpy(P).to(dev), torch.from_numpy(depth).to(dev))
+    g = out.float().cpu().numpy()
+    o = oracle.rope_neox(x, P, depth, out_bf16=(out_dtype == "bf16"))
+    mag = np.abs(x[..., :half]) + np.abs(x[..., half:])
+    bound = ulp(o, out_dtype) + np.exp2(-50.0) * np.concatenate([mag, mag], axis=-1)
+    assert np.all(np.abs(g - o) <= bound), float(np.max(np.abs(g - o) / bound))

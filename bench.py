@@ -10,7 +10,11 @@ Metric: algorithmic attention TFLOP/s of the whole step (visible (row, key) pair
 2*(2*d_latent + d_rope) flops per pair and head), with HBM GB/s and the roofline
 fraction of the attention kernel beside it.  Inputs are resident in HBM when the timed
 region starts; between steps a 256 MB buffer is written so that every step starts with
-a cold L2; each step is timed with CUDA events on the launching stream.
+a cold L2; each step is timed with CUDA events on the launching stream.  The timed steps
+replay two CUDA graphs captured once from the step's calls (visibility + both RoPE calls;
+the attention call), so the same kernels run with the same arguments without the host's
+per-call work; --eager times the plain calls instead.  The end-to-end figure (host
+buffers, copies inside the timed region) always uses the plain calls.
 
 --impl reference times the float64 CPU oracle (the repository's own reference
 implementation of the same step) on a bounded sample of the workload per step.

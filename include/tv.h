@@ -24,6 +24,10 @@
  *     The library allocates no device memory; scratch is a caller-provided workspace.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *     The return value reports synchronous argument checks and launch errors only.
+ *   - Calls make no synchronising CUDA call, so they can be captured into a CUDA graph on
+ *     a capturing stream.  The first call in a process (or on a new device) does one-time
+ *     set-up (occupancy query, driver entry points); make it outside a capture.  A graph
+ *     keeps the call's arguments, sizes and workspace as they were when it was captured.
  *   - Data-dependent errors found on the device (an invalid parent array, a prefix that
  *     does not fit the cache geometry, a device wait that ran out) are stored as a
  *     negative tv_status into *status, a caller-owned device int32.  The library never

@@ -159,31 +159,6 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
       : "memory");
 }
-// 3-D tile load delivered to every CTA of the cluster named in `mask`, at the same shared
-// offset in each, signalling the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorMap* map, int c0,
-                                                      int c1, int c2, uint64_t* bar,
-                                                      uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-// Ask the TMA engine to bring a box into L2 without delivering it to shared memory.
-__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                   int c3, int c4) {
-  asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
-                   map),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-               : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                   int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(map),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -203,25 +178,6 @@ __device__ __forceinline__ void bulk_commit() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Asynchronous stores into a peer CTA's shared memory (cluster addresses).  Each one
-// performs a complete_tx of its size on the peer's mbarrier `bar_cluster` (which must live
-// in the same CTA as the destination); that completion has release semantics at cluster
-// scope, so a thread that waits on the barrier sees the data.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d, uint32_t bar_cluster) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
-      : "memory");
-}
-__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
-                                             uint32_t bar_cluster) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                   cluster_addr),
-               "r"(v), "r"(bar_cluster)
-               : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

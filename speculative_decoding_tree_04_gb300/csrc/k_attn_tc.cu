@@ -700,8 +700,9 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
           // arm the buffer's next phase now: its next message is only sent after the MMAs
           // below have read this one
           mbar_arrive_expect_tx(&sh.p_full[pb], kMsgBytes);
-          // the message arrived through generic-proxy stores; the MMAs read it through the
-          // async proxy
+          // The message arrived by a bulk copy, in the async proxy the MMAs read through, so
+          // this fence is not required for ordering; a variant without it (flags loaded
+          // before the re-arm) measured about 1 % slower, so it stays.
           fence_proxy_async_smem();
           const uint32_t flags =
               *reinterpret_cast<volatile uint32_t*>(inbox + pb * kMsgStride + kMsgFlags);

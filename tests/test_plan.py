@@ -1,0 +1,113 @@
+"""Host-side planning of tv_verify_attn (CPU only: no kernel is launched).
+
+The kernel family, the number of kernels a call enqueues and the workspace it asks for are
+decided on the host from the argument struct.  These tests check the documented rules:
+
+  * TV_PATH_AUTO takes the tensor cores for bf16 queries and cache with d_latent 512,
+    d_rope 64 and at least 256 (row, head) rows, and the CUDA cores otherwise;
+  * a tensor-core call enqueues work preparation + attention, plus a key gather when a
+    paged cache's keys exceed 64 MB, plus a combine when the keys are split;
+  * the workspace has room for what the plan keeps there (split partial outputs, the
+    gathered key copy), and a call refuses a workspace that is too small or misaligned
+    before it launches anything.
+"""
+import ctypes
+
+import pytest
+
+from speculative_decoding_tree_04_gb300 import tv
+
+FAKE = 1 << 20  # placeholder device address; planning never dereferences it
+
+
+def args(B, H, Q, max_prefix, paged=False, dt=tv.TV_BF16, num_splits=0, path=tv.PATH_AUTO):
+    a = tv.AttnArgs()
+    a.struct_size = ctypes.sizeof(tv.AttnArgs)
+    a.B, a.H, a.Q, a.d_latent, a.d_rope = B, H, Q, 512, 64
+    a.scale = 0.07
+    a.q_dt = a.kv_dt = dt
+    a.q_latent = a.q_pe = a.c_kv = a.k_pe = a.prefix_len = a.anc = a.out = a.lse = FAKE
+    a.ckv_row_stride, a.kpe_row_stride = 512, 64
+    kv = max_prefix + Q
+    if paged:
+        pages = (kv + 63) // 64
+        a.cache = tv.CacheLayout(FAKE, 64, pages, 0, B * pages * 64)
+    else:
+        a.cache = tv.CacheLayout(None, 64, 0, kv, B * kv)
+    a.max_prefix_len = max_prefix
+    a.num_splits = num_splits
+    a.path = path
+    return a
+
+
+def lib():
+    return tv.load()
+
+
+def path(a):
+    return lib().tv_verify_attn_path(ctypes.byref(a))
+
+
+def launches(a):
+    return lib().tv_verify_attn_launches(ctypes.byref(a))
+
+
+def workspace(a):
+    return lib().tv_verify_attn_workspace_size(ctypes.byref(a))
+
+
+def test_auto_path_by_shape_and_dtype(tvlib):
+    assert path(args(32, 64, 33, 8192)) == tv.PATH_TCGEN05
+    assert path(args(8, 64, 9, 4096, paged=True)) == tv.PATH_TCGEN05
+    assert path(args(2, 16, 17, 2048, dt=tv.TV_F32)) == tv.PATH_SIMT
+    assert path(args(1, 8, 5, 1)) == tv.PATH_SIMT            # 40 rows: too few for tiles
+    assert path(args(1, 8, 5, 1, path=tv.PATH_TCGEN05)) == tv.PATH_TCGEN05
+    a = args(2, 16, 17, 2048, dt=tv.TV_F32, path=tv.PATH_TCGEN05)
+    assert path(a) == tv.TV_ERR_UNSUPPORTED                   # fp32 has no tensor-core path
+
+
+def test_tensor_core_launch_structure(tvlib):
+    # many row tiles and a contiguous cache: preparation + attention
+    assert launches(args(32, 64, 33, 8192)) == 2
+    # a forced split adds the combine
+    assert launches(args(32, 64, 33, 8192, num_splits=3)) == 3
+    # a paged cache of 32 x 8225 keys (about 300 MB of keys) adds the key gather
+    assert launches(args(32, 64, 33, 8192, paged=True)) == 3
+    assert launches(args(32, 64, 33, 8192, paged=True, num_splits=2)) == 4
+    # a paged cache of 8 x 4105 keys (about 38 MB) keeps per-step tensor maps: no gather
+    assert launches(args(8, 64, 9, 4096, paged=True, num_splits=1)) == 2
+
+
+def test_few_row_tiles_split_the_keys(tvlib):
+    # 8 sequences x 5 row tiles cannot fill the GPU's clusters: the plan splits the keys,
+    # which adds the combine kernel
+    assert launches(args(8, 64, 9, 4096, paged=True)) == 3
+    # a short prefix is not split (each split would be under two 128-key steps)
+    assert launches(args(8, 64, 9, 100)) == 2
+
+
+def test_workspace_holds_what_the_plan_keeps_there(tvlib):
+    rows = 32 * 33 * 64
+    base = workspace(args(32, 64, 33, 8192))
+    assert 0 < base < (1 << 20)                               # work records only
+    ws2 = workspace(args(32, 64, 33, 8192, num_splits=2))
+    ws4 = workspace(args(32, 64, 33, 8192, num_splits=4))
+    assert ws2 >= 2 * rows * (512 + 1) * 4                    # partial outputs + lse
+    assert ws4 >= 4 * rows * (512 + 1) * 4 and ws4 > ws2
+    gathered = workspace(args(32, 64, 33, 8192, paged=True))
+    assert gathered >= 32 * 8225 * (512 + 64) * 2             # contiguous key copy
+    maps = workspace(args(8, 64, 9, 4096, paged=True, num_splits=1))
+    assert maps >= 8 * ((4105 + 127) // 128) * 256            # two 128-byte maps per step
+    assert maps < 8 * 4105 * (512 + 64) * 2                   # and no key copy
+    for size in (base, ws2, gathered, maps):
+        assert size % 256 == 0
+
+
+@pytest.mark.parametrize("offset,short", [(128, False), (0, True)])
+def test_call_refuses_a_bad_workspace_before_launching(tvlib, offset, short):
+    a = args(32, 64, 33, 8192, num_splits=2)
+    need = workspace(a)
+    ws_bytes = need - 256 if short else need
+    rc = lib().tv_verify_attn(ctypes.byref(a), ctypes.c_void_p(FAKE + offset), ws_bytes, None)
+    assert rc == tv.TV_ERR_WORKSPACE
+    assert lib().tv_last_error()

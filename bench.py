@@ -155,6 +155,17 @@ def source_sha(filename: str | None = None):
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(values, pg, device):
+    """Each entry's largest value over all ranks (a job's step time is its slowest rank's).
+    pg is torch.distributed (initialised) or None for a single process."""
+    if pg is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -309,10 +320,7 @@ def main():
     attn_ms = [a0.elapsed_time(a1) for _, a0, a1, _ in ev]
     ms = float(np.sum(step_ms)) / args.steps
     ams = float(np.sum(attn_ms)) / args.steps
-    if pg is not None:
-        t = torch.tensor([ms, ams], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, ams = float(t[0]), float(t[1])
+    ms, ams = max_over_ranks([ms, ams], pg, dev)
 
     if args.quick:
         if rank == 0:
@@ -357,10 +365,7 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], pg, dev)
 
     if rank != 0:
         pg.destroy_process_group() if pg is not None else None

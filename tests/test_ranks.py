@@ -1,0 +1,74 @@
+"""Multi-rank host logic of bench.py on CPU (gloo, two ranks; no GPU).
+
+The step has no cross-GPU exchange: with N ranks every rank runs its own replica, the job's
+step time is the slowest rank's, and only rank 0 prints.  These tests run that reduction
+over a real two-rank gloo group and the reference arm's rank handling in subprocesses.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        got = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 0.25], dist, torch.device("cpu"))
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res[0] == res[1] == [2.0, 5.0, 0.25]
+
+
+def test_max_over_ranks_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([3, 1.5], None, None) == [3.0, 1.5]
+
+
+def _reference_arm(rank):
+    env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2",
+               MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    return subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                           "--workload", "cfg1_fp32", "--steps", "1", "--warmup", "3"],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+
+
+def test_reference_arm_only_rank0_prints():
+    r1 = _reference_arm(1)
+    assert r1.returncode == 0, r1.stderr[-2000:]
+    assert r1.stdout.strip() == ""
+    r0 = _reference_arm(0)
+    assert r0.returncode == 0, r0.stderr[-2000:]
+    line = json.loads(r0.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"

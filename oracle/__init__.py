@@ -24,8 +24,11 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tv_oracle.c")
+_SRC_TREE = os.path.join(_HERE, "tree_oracle.c")
+_SOURCES = {"tv": _SRC, "tree": _SRC_TREE}
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
+_CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared"]
 
 OK, ERR_INVALID_ARG, ERR_INVALID_TREE, ERR_UNSUPPORTED = 0, -1, -2, -3
 
@@ -35,11 +38,12 @@ class OracleError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    """Compile tv_oracle.c into liboracle.so next to it (gcc, OpenMP, no FP contraction)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    """Compile the oracle's C sources into liboracle.so next to them (gcc, OpenMP, no FP
+    contraction)."""
+    newest = max(os.path.getmtime(f) for f in _SOURCES.values())
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-               _SRC, "-o", tmp, "-lm"]
+        cmd = ["gcc", *_CFLAGS, *_SOURCES.values(), "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -57,6 +61,11 @@ def _bind(path):
     lib.tvo_bf16_round.argtypes = [ctypes.c_float]
     lib.tvo_bf16_round.restype = ctypes.c_float
     lib.tvo_max_threads.restype = ctypes.c_int
+    lib.tvo_set_threads.argtypes = [i32]
+    lib.tro_argmax_rows.argtypes = [P, i64, i64, i64, P]
+    lib.tro_tree_accept.argtypes = [P, P, P, i32, i32, P, P, P]
+    lib.tro_compact_kv.argtypes = [P, i64, P, i64, i32, i32, P, i32, i32, i64, P, P, P, i32,
+                                   i32, P]
     return lib
 
 
@@ -67,19 +76,20 @@ def _load():
     return _lib
 
 
-def compile_variant(src_text: str, out_path: str) -> str:
-    """Compile an edited copy of the oracle source (used by tests that plant a mistake in
-    the oracle to show that the pins catch it).  Returns the library path."""
+def compile_variant(src_text: str, out_path: str, which: str = "tv") -> str:
+    """Compile the oracle with an edited copy of one of its sources (``which``: "tv" for
+    tv_oracle.c, "tree" for tree_oracle.c); used by tests that plant a mistake in the
+    oracle to show that the pins catch it.  Returns the library path."""
     src = out_path + ".c"
     with open(src, "w") as f:
         f.write(src_text)
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC",
-                    "-shared", src, "-o", out_path, "-lm"], check=True)
+    others = [v for k, v in _SOURCES.items() if k != which]
+    subprocess.run(["gcc", *_CFLAGS, src, *others, "-o", out_path, "-lm"], check=True)
     return out_path
 
 
-def source_text() -> str:
-    with open(_SRC) as f:
+def source_text(which: str = "tv") -> str:
+    with open(_SOURCES[which]) as f:
         return f.read()
 
 
@@ -116,6 +126,11 @@ def _check(rc, what):
 
 def max_threads() -> int:
     return int(_load().tvo_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's later OpenMP regions (for timing only)."""
+    _load().tvo_set_threads(int(n))
 
 
 def visibility(parent, want_anc=True):
@@ -218,3 +233,52 @@ def tree_verify_step(inp, seqs=None, nthreads=0):
                            inp["kv_stride_b"], seqs=seqs, nthreads=nthreads)
     return dict(vis=vis, depth=depth, anc=anc, q_pe_rot=q_pe_rot, kpe_tree_rot=kpe_rot,
                 k_pe_cache=k_pe_cache, out=out, lse=lse)
+
+
+# ---- greedy tree acceptance and post-verify compaction (tree_oracle.c) --------------
+
+def argmax_rows(logits):
+    """logits [..., V] float32 -> int32 argmax of every row (smallest index on ties)."""
+    x = _c(logits, np.float32)
+    V = x.shape[-1]
+    rows = x.size // V
+    out = np.empty(x.shape[:-1], np.int32)
+    rc = _load().tro_argmax_rows(_ptr(x), rows, V, V, _ptr(out))
+    _check(rc, "argmax_rows")
+    return out
+
+
+def tree_accept(parent, tokens, target):
+    """Greedy acceptance: returns (accept_len [B], path [B,Q], new_tokens [B,Q]) int32."""
+    parent = _c(parent, np.int32)
+    B, Q = parent.shape
+    acc = np.zeros(B, np.int32)
+    path = np.zeros((B, Q), np.int32)
+    emit = np.zeros((B, Q), np.int32)
+    rc = _load().tro_tree_accept(_ptr(parent), _ptr(_c(tokens, np.int32)),
+                                 _ptr(_c(target, np.int32)), B, Q, _ptr(acc), _ptr(path),
+                                 _ptr(emit))
+    if rc != OK:
+        err = OracleError(f"tree_accept failed with status {rc}")
+        err.status = rc
+        raise err
+    return acc, path, emit
+
+
+def compact_kv(c_kv, k_pe, prefix_len, path, accept_len, page_table=None, page_size=64,
+               kv_stride_b=0):
+    """Post-verify compaction on copies of the cache arrays: returns (c_kv, k_pe,
+    new_prefix_len)."""
+    ck = np.array(c_kv, dtype=np.float32, copy=True, order="C")
+    kp = np.array(k_pe, dtype=np.float32, copy=True, order="C")
+    path = _c(path, np.int32)
+    B, Q = path.shape
+    pt = None if page_table is None else _c(page_table, np.int32)
+    maxp = 0 if pt is None else pt.shape[1]
+    newp = np.zeros(B, np.int32)
+    rc = _load().tro_compact_kv(_ptr(ck), ck.shape[1], _ptr(kp), kp.shape[1], ck.shape[1],
+                                kp.shape[1], _ptr(pt), int(page_size), int(maxp),
+                                int(kv_stride_b), _ptr(_c(prefix_len, np.int32)), _ptr(path),
+                                _ptr(_c(accept_len, np.int32)), B, Q, _ptr(newp))
+    _check(rc, "compact_kv")
+    return ck, kp, newp

@@ -295,6 +295,15 @@ int tvo_verify_attn(int B, int H, int Q, int DL, int DR, double scale,
   return TVO_OK;
 }
 
+/* Threads of later parallel regions (n <= 0: leave as is); for the CPU-baseline timing. */
+void tvo_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Number of OpenMP threads a parallel region would use (for the CPU-baseline report). */
 int tvo_max_threads(void) {
 #ifdef _OPENMP

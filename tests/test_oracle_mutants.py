@@ -10,6 +10,7 @@ unnoticed.
 import pytest
 
 import oracle
+from tests import test_oracle_accept as TAC
 from tests import test_oracle_attn as TA
 from tests import test_oracle_rope as TR
 from tests import test_oracle_visibility as TV
@@ -52,6 +53,55 @@ PINS = [
     TA.test_dominant_score_selects_row_and_ones_give_one, TA.test_golden_worked_example,
     TA.test_full_step_chain_equals_rope_then_causal_attention,
 ]
+
+
+# planted mistakes in the acceptance / compaction oracle (tree_oracle.c)
+TREE_MUTANTS = {
+    "argmax_ties_to_largest": ("if (x[v] > x[best]) best = v;", "if (x[v] >= x[best]) best = v;"),
+    "accept_compares_child_target": ("if (par[c] == cur && tok[c] == tgt[cur]) {",
+                                     "if (par[c] == cur && tok[c] == tgt[c]) {"),
+    "accept_any_node_not_child": ("if (par[c] == cur && tok[c] == tgt[cur]) {",
+                                  "if (c > cur && tok[c] == tgt[cur]) {"),
+    "accept_largest_child": ("next = c; /* the smallest qualifying child */\n          break;",
+                             "next = c; /* the smallest qualifying child */"),
+    "bonus_from_root": ("emit[a] = tgt[cur]; /* bonus token */", "emit[a] = tgt[0];"),
+    "compact_dst_off_by_one": ("b, P + d);", "b, P + d + 1);"),
+    "compact_prefix_misses_root": ("new_prefix_len[b] = (int32_t)(P + 1 + a);",
+                                   "new_prefix_len[b] = (int32_t)(P + a);"),
+    "compact_skips_k_pe": ("memcpy(k_pe + dst * kpe_stride, k_pe + src * kpe_stride,",
+                           "if (0) memcpy(k_pe + dst * kpe_stride, k_pe + src * kpe_stride,"),
+}
+
+TREE_PINS = [
+    TAC.test_argmax_matches_numpy_and_takes_smallest_index_on_ties,
+    TAC.test_brute_force_all_six_node_trees, TAC.test_chain_accepts_up_to_first_mismatch,
+    TAC.test_star_accepts_at_most_one_and_duplicate_siblings_take_smallest_index,
+    TAC.test_speculative_output_equals_autoregressive_output, TAC.test_golden_worked_example,
+    lambda: TAC.test_compaction_equals_out_of_place_gather(False),
+    lambda: TAC.test_compaction_equals_out_of_place_gather(True),
+]
+
+
+@pytest.mark.parametrize("name", sorted(TREE_MUTANTS))
+def test_tree_pins_catch_planted_mistake(name, tmp_path):
+    src = oracle.source_text("tree")
+    old, new = TREE_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor not found for {name}"
+    path = oracle.compile_variant(src.replace(old, new), str(tmp_path / f"mut_{name}.so"),
+                                  which="tree")
+    failures = 0
+    with oracle.use_library(path):
+        for pin in TREE_PINS:
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError):
+                failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
+
+
+def test_unmutated_tree_oracle_passes_all_pins():
+    for pin in TREE_PINS:
+        pin()
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -173,20 +173,47 @@ def dist_env():
     return rank, world, local
 
 
-def cpu_baseline(inp, seqs, repeat=1):
-    import oracle
-    from speculative_decoding_tree_04_gb300 import synth  # noqa: F401
-    oracle.build()
-    t0 = time.perf_counter()
-    for _ in range(repeat):
-        oracle.tree_verify_step(inp, seqs=seqs)
-    dt = (time.perf_counter() - t0) / repeat
+def _subset(inp, seqs):
     sub = dict(inp)
     sub["B"] = len(seqs)
     sub["parent"] = inp["parent"][seqs]
     sub["prefix_len"] = inp["prefix_len"][seqs]
-    fl, by, _ = work_of(sub)
-    return dt, fl, by, oracle.max_threads()
+    return sub
+
+
+def cpu_baseline(inp, seqs, nthreads=0):
+    """One oracle step (visibility, RoPE of the queries, RoPE of the tree keys written into
+    the cache, attention) on sequences ``seqs``, each call timed.  Returns (seconds,
+    flops, bytes, threads used, per-call seconds)."""
+    import oracle
+    oracle.build()
+    threads = nthreads if nthreads > 0 else (os.cpu_count() or 1)
+    oracle.set_threads(threads)
+    P = inp["prefix_len"]
+    t = {}
+    t0 = time.perf_counter()
+    vis, depth, anc = oracle.visibility(inp["parent"])
+    t["visibility"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    q_pe_rot = oracle.rope_neox(inp["q_pe"][seqs], P[seqs], depth[seqs], inp["rope_base"],
+                                out_bf16=inp["q_dtype"] == "bf16")
+    t["rope_q"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    kpe_rot = oracle.rope_neox(inp["kpe_tree"][:, :, None, :], P, depth, inp["rope_base"],
+                               out_bf16=inp["kv_dtype"] == "bf16")[:, :, 0, :]
+    k_pe_cache = oracle.scatter_tree_kpe(kpe_rot, inp["k_pe"], P, inp.get("page_table"),
+                                         inp["page_size"], inp["kv_stride_b"])
+    t["rope_k"] = time.perf_counter() - t0
+    q_full = np.zeros_like(inp["q_pe"])
+    q_full[seqs] = q_pe_rot
+    t0 = time.perf_counter()
+    oracle.verify_attn(inp["q_latent"], q_full, inp["c_kv"], k_pe_cache, P, vis, inp["scale"],
+                       inp.get("page_table"), inp["page_size"], inp["kv_stride_b"], seqs=seqs,
+                       nthreads=threads)
+    t["attention"] = time.perf_counter() - t0
+    dt = sum(t.values())
+    fl, by, _ = work_of(_subset(inp, seqs))
+    return dt, fl, by, oracle.max_threads(), t
 
 
 def run_reference(args, inp, rank, world):
@@ -194,13 +221,14 @@ def run_reference(args, inp, rank, world):
     if rank != 0:
         return
     seqs = synth.sample_sequences(inp, args.ref_seqs)
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        pass
+    for _ in range(args.warmup):          # untimed warm-up steps on the same sample
+        cpu_baseline(inp, seqs)
     times = []
     fl = by = 0
     threads = 1
+    per = {}
     for _ in range(args.steps):
-        dt, fl, by, threads = cpu_baseline(inp, seqs)
+        dt, fl, by, threads, per = cpu_baseline(inp, seqs)
         times.append(dt)
     t = float(np.mean(times))
     val = fl / t / 1e12
@@ -211,7 +239,8 @@ def run_reference(args, inp, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "sample": f"{len(seqs)} of {inp['B']} sequences"},
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"sequences {list(map(int, seqs))} of {args.workload}"},
+                         "sample": f"sequences {list(map(int, seqs))} of {args.workload}",
+                         "per_call_s": {k: round(v, 4) for k, v in per.items()}},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -219,6 +248,85 @@ def run_reference(args, inp, rank, world):
 
 
 METRIC = "tree-verify attn TFLOP/s and HBM GB/s per GB300, % of binding roofline"
+
+
+def relaunch_ranks(n):
+    """``--gpus N`` without a launcher: start N ranks of this same command through
+    torch.distributed.run (one process per GPU, rendezvous on 127.0.0.1) and return its
+    exit code."""
+    import socket
+    with socket.socket() as sck:
+        sck.bind(("127.0.0.1", 0))
+        port = sck.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def roofline_of(path, tv, flops, byts, ams, peaks, clk, kernel_tag, workload, dev):
+    import torch
+    attn_tflops = flops / (ams * 1e-3) / 1e12
+    attn_gbs = byts / (ams * 1e-3) / 1e9
+    if path == tv.PATH_TCGEN05:
+        roof = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
+                "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS bf16_tflops)"}
+    else:
+        props = torch.cuda.get_device_properties(dev)
+        mhz = (clk or {}).get("sm_max_mhz", 2070.0)
+        alu = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": attn_tflops, "peak": alu, "unit": "TFLOP/s",
+                "frac": attn_tflops / alu,
+                "peak_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {mhz} MHz"}
+    trf = kernel_traffic(kernel_tag, workload)
+    roof["traffic"] = None if trf is None else trf["dram_bytes_per_launch"]
+    roof["algorithmic_bytes"] = byts
+    roof["hbm_gbs_achieved"] = attn_gbs
+    roof["hbm_frac"] = attn_gbs / peaks["hbm_gbs"]
+    roof["kernel_ms"] = ams
+    return roof
+
+
+def time_steps(step, steps, warmup, eager, flush, dev, barrier, cold=True):
+    """Time `steps` verify steps (CUDA events on the launching stream) after `warmup`
+    untimed ones.  cold: write the L2-sized flush buffer before every step (outside the
+    events).  Returns (mean step ms, mean attention-call ms, graphs)."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    graphs = None if eager else step.capture_graphs()
+    for _ in range(warmup):
+        if graphs is None:
+            step.run()
+        else:
+            graphs[0].replay()
+            graphs[1].replay()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for k in range(steps):
+        if cold:
+            flush.add_(1.0)
+        s0, a0, a1, s1 = ev[k]
+        s0.record(stream)
+        if graphs is None:
+            step.visibility()
+            step.rope_q()
+            step.rope_k()
+        else:
+            graphs[0].replay()
+        a0.record(stream)
+        if graphs is None:
+            step.attention()
+        else:
+            graphs[1].replay()
+        a1.record(stream)
+        s1.record(stream)
+    barrier()
+    ms = float(np.sum([s0.elapsed_time(s1) for s0, _, _, s1 in ev])) / steps
+    ams = float(np.sum([a0.elapsed_time(a1) for _, a0, a1, _ in ev])) / steps
+    return ms, ams, graphs
 
 
 def main():
@@ -236,15 +344,23 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller profiler captures)")
+    ap.add_argument("--also", default=None,
+                    help="comma-separated further workloads timed the same way and reported "
+                         "under 'configs' (default: cfg4_bf16 beside cfg5_bf16)")
     ap.add_argument("--quick", action="store_true",
                     help="device-timed steps only (no end-to-end pass, no CPU baseline); "
                          "used for profiler runs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    rank, world, local = dist_env()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_ranks(args.gpus))
+    if world != args.gpus:
+        raise SystemExit(f"bench: --gpus {args.gpus} but WORLD_SIZE={world}")
+
     from speculative_decoding_tree_04_gb300 import synth
 
-    rank, world, local = dist_env()
     inp = synth.generate(args.workload, **({"B": args.batch} if args.batch > 0 else {}))
     if args.impl == "reference":
         run_reference(args, inp, rank, world)
@@ -279,47 +395,14 @@ def main():
     # The timed steps replay two CUDA graphs of the step's calls (captured once; the same
     # kernels and arguments as the plain calls, without the host's per-call work), unless
     # --eager asks for the plain calls.
-    graphs = None if args.eager else step.capture_graphs()
-    for _ in range(args.warmup):
-        if graphs is None:
-            step.run()
-        else:
-            graphs[0].replay()
-            graphs[1].replay()
-    barrier()
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     barrier()
     t_wall0 = time.perf_counter()
-    for k in range(args.steps):
-        flush.add_(1.0)                     # cold L2 for every step (outside the events)
-        s0, a0, a1, s1 = ev[k]
-        s0.record(stream)
-        if graphs is None:
-            step.visibility()
-            step.rope_q()
-            step.rope_k()
-        else:
-            graphs[0].replay()
-        a0.record(stream)
-        if graphs is None:
-            step.attention()
-        else:
-            graphs[1].replay()
-        a1.record(stream)
-        s1.record(stream)
-    barrier()
+    ms, ams, graphs = time_steps(step, args.steps, args.warmup, args.eager, flush, dev, barrier)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
-    step_ms = [s0.elapsed_time(s1) for s0, _, _, s1 in ev]
-    attn_ms = [a0.elapsed_time(a1) for _, a0, a1, _ in ev]
-    ms = float(np.sum(step_ms)) / args.steps
-    ams = float(np.sum(attn_ms)) / args.steps
     ms, ams = max_over_ranks([ms, ams], pg, dev)
 
     if args.quick:
@@ -332,16 +415,19 @@ def main():
             pg.destroy_process_group()
         return
 
+    # warm L2: the same steps without the flush between them (reported beside the cold)
+    _, ams_warm, _ = time_steps(step, args.steps, 1, args.eager, flush, dev, barrier, cold=False)
+    (ams_warm,) = max_over_ranks([ams_warm], pg, dev)
+
     # ---- end to end through the public calls, host buffers in pinned memory ----------
     host = {k: _dev_float(inp, k, dev, pin=True) for k in
             ("q_latent", "q_pe", "kpe_tree", "c_kv", "k_pe")}
-    import torch as _t
-    host_int = {"parent": _t.from_numpy(inp["parent"]).pin_memory(),
-                "prefix_len": _t.from_numpy(inp["prefix_len"]).pin_memory()}
+    host_int = {"parent": torch.from_numpy(inp["parent"]).pin_memory(),
+                "prefix_len": torch.from_numpy(inp["prefix_len"]).pin_memory()}
     if inp["page_table"] is not None:
-        host_int["page_table"] = _t.from_numpy(inp["page_table"]).pin_memory()
-    out_h = _t.empty(step.out.shape, dtype=_t.float32).pin_memory()
-    lse_h = _t.empty(step.lse.shape, dtype=_t.float32).pin_memory()
+        host_int["page_table"] = torch.from_numpy(inp["page_table"]).pin_memory()
+    out_h = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_int.values()))
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
     dst = {"q_latent": step.q_latent, "q_pe": step.q_pe_raw, "kpe_tree": step.kpe_tree,
@@ -366,43 +452,59 @@ def main():
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     (e2e_ms,) = max_over_ranks([e2e_ms], pg, dev)
+    launches = step.launches_per_step() * args.steps
+    del step, host, host_int, graphs
+    torch.cuda.empty_cache()
+
+    # ---- further workloads, the same protocol (reported under "configs") ------------
+    also = args.also
+    if also is None:
+        also = "cfg4_bf16" if args.workload == "cfg5_bf16" and args.batch == 0 else ""
+    peaks = load_peaks()
+    configs = {}
+    for name in [w for w in also.split(",") if w]:
+        inp2 = synth.generate(name)
+        st2 = VerifyStep(inp2, device=dev, path=args.path)
+        p2 = st2.chosen_path()
+        fl2, by2, _ = work_of(inp2)
+        ms2, ams2, _ = time_steps(st2, args.steps, args.warmup, args.eager, flush, dev, barrier)
+        _, ams2w, _ = time_steps(st2, args.steps, 1, args.eager, flush, dev, barrier, cold=False)
+        ms2, ams2, ams2w = max_over_ranks([ms2, ams2, ams2w], pg, dev)
+        tag2 = "attn_tc" if p2 == tv.PATH_TCGEN05 else "attn_simt"
+        configs[name] = {
+            "ms_per_step": ms2, "attn_ms": ams2, "attn_ms_warm_l2": ams2w,
+            "value": fl2 / (ms2 * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+            "path": ["auto", "simt", "tcgen05"][p2], "launches_per_step": st2.launches_per_step(),
+            "roofline": roofline_of(p2, tv, fl2, by2, ams2, peaks, clk, tag2, name, dev),
+            "source_sha": source_sha(KERNEL_FILES[tag2]),
+        }
+        del st2
+        torch.cuda.empty_cache()
 
     if rank != 0:
         pg.destroy_process_group() if pg is not None else None
         return
 
-    peaks = load_peaks()
     tflops = flops / (ms * 1e-3) / 1e12 * world
-    attn_tflops = flops / (ams * 1e-3) / 1e12
     attn_gbs = byts / (ams * 1e-3) / 1e9
     kernel_tag = "attn_tc" if path == tv.PATH_TCGEN05 else "attn_simt"
-    trf = kernel_traffic(kernel_tag, args.workload)
-    if path == tv.PATH_TCGEN05 or inp["kv_dtype"] == "bf16":
-        roof = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"],
-                "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS bf16_tflops)"}
-    else:
-        props = torch.cuda.get_device_properties(dev)
-        mhz = (clk or {}).get("sm_max_mhz", 2070.0)
-        alu = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": attn_tflops, "peak": alu, "unit": "TFLOP/s",
-                "frac": attn_tflops / alu,
-                "peak_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 x {mhz} MHz"}
-    roof["traffic"] = None if trf is None else trf["dram_bytes_per_launch"]
-    roof["algorithmic_bytes"] = byts
-    roof["hbm_gbs_achieved"] = attn_gbs
-    roof["hbm_frac"] = attn_gbs / peaks["hbm_gbs"]
-    roof["kernel_ms"] = ams
+    roof = roofline_of(path, tv, flops, byts, ams, peaks, clk, kernel_tag, args.workload, dev)
 
     cpu = None
-    if not args.no_cpu_baseline and world >= 1:
+    if not args.no_cpu_baseline:
         seqs = synth.sample_sequences(inp, args.ref_seqs)
-        dt, fl, by, thr = cpu_baseline(inp, seqs)
+        dt, fl, by, thr, per = cpu_baseline(inp, seqs)
+        one = seqs[:1]
+        dt1, fl1, _, thr1, per1 = cpu_baseline(inp, one, nthreads=1)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                "sample": f"full step (visibility, RoPE, attention) of sequences "
-                         f"{list(map(int, seqs))} of {args.workload}, {dt:.1f} s"}
+                         f"{list(map(int, seqs))} of {args.workload}, {dt:.1f} s",
+               "per_call_s": {k: round(v, 4) for k, v in per.items()},
+               "single_thread": {"value": fl1 / dt1 / 1e12, "unit": "TFLOP/s", "cores": thr1,
+                                 "sample": f"sequence {int(one[0])} of {args.workload}, "
+                                           f"{dt1:.1f} s",
+                                 "per_call_s": {k: round(v, 4) for k, v in per1.items()}}}
 
-    launches = step.launches_per_step() * args.steps
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -415,13 +517,15 @@ def main():
                    if args.workload == "cfg5_bf16" else f"mean {float(inp['prefix_len'].mean()):.0f}",
                    "paged": inp["page_table"] is not None, "path": ["auto", "simt", "tcgen05"][path],
                    "l2": "256 MB buffer written between steps (cold L2); per-step CUDA events",
-                   "launch": "eager calls" if graphs is None else
+                   "launch": "eager calls" if args.eager else
                    "CUDA graphs of the calls (visibility+RoPE, attention), captured once",
                    "e2e_launch": "eager calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_gbs": attn_gbs,
         "attn_ms": ams,
+        "attn_ms_warm_l2": ams_warm,
         "roofline": roof,
+        "configs": configs,
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

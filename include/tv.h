@@ -64,6 +64,13 @@ typedef enum { TV_F32 = 0, TV_BF16 = 1 } tv_dtype;
  * run the request. */
 typedef enum { TV_PATH_AUTO = 0, TV_PATH_SIMT = 1, TV_PATH_TCGEN05 = 2 } tv_path;
 
+/* How the tensor-core path reads a paged cache.  AUTO copies the pages into a contiguous
+ * key view in the workspace when the keys exceed 64 MB and builds per-step tensor maps
+ * into the pages otherwise; the other two force one form (tests use them to run both
+ * forms on small caches).  Ignored by the CUDA-core path and by contiguous caches.
+ * TV_PAGED_GATHER needs B * (max_prefix_len + Q rounded up to 128) < 2^31 rows. */
+typedef enum { TV_PAGED_AUTO = 0, TV_PAGED_STEP_MAPS = 1, TV_PAGED_GATHER = 2 } tv_paged_view;
+
 /*
  * Geometry of the latent KV cache.  Logical key j (0 <= j < prefix_len[b] + Q) of
  * sequence b lives in cache row
@@ -172,6 +179,7 @@ typedef struct {
   int32_t* status;          /* device int32, nullable (see conventions) */
   int32_t path;             /* tv_path; TV_PATH_AUTO normally */
   int32_t num_splits;       /* 0 = automatic; else force this many KV splits */
+  int32_t paged_view;       /* tv_paged_view; TV_PAGED_AUTO normally */
 } tv_attn_args;
 
 /* Bytes of workspace tv_verify_attn needs for these arguments (0 if none).  The size
@@ -214,10 +222,15 @@ int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void
  * that loads it, held until the process exits.  It never allocates.  The caller still
  * passes every input and output through `a`.
  *   - The first call on a device looks up the array's address on that device (a
- *     cudaGetSymbolAddress); make that first call before any stream capture.
- *   - A request whose scratch need (tv_verify_attn_workspace_size(a) for the CUDA-core
- *     path) exceeds TV_NOALLOC_SCRATCH_BYTES returns TV_ERR_WORKSPACE with an explanation
- *     in tv_last_error().
+ *     cudaGetSymbolAddress), whatever the request; so does the first call after the
+ *     device's CUDA context changed (cudaDeviceReset, or another context made current),
+ *     since the array then lives in a newly loaded module.  Make such a first call before
+ *     any stream capture.
+ *   - A request whose scratch need exceeds TV_NOALLOC_SCRATCH_BYTES returns
+ *     TV_ERR_WORKSPACE with an explanation in tv_last_error().  The need is what
+ *     tv_verify_attn_workspace_size(a) reports for the same arguments with
+ *     a->path = TV_PATH_SIMT (with TV_PATH_AUTO on a tensor-core shape that query reports
+ *     the tensor-core path's size instead).
  *   - All calls share the one array and it keeps the last call's contents (nothing in it
  *     needs to start at zero).  Calls whose kernels can overlap on the GPU -- unordered
  *     streams, several host threads -- race on it; the caller must serialise them.

@@ -62,6 +62,7 @@
 
 #include "sm100_ptx.h"
 #include "tv_internal.h"
+#include "tv_testing.h"
 
 namespace tv {
 namespace {
@@ -95,7 +96,8 @@ constexpr int kSideB = kInboxOff + kNInbox * kMsgStride;
 constexpr int kSideMax = kSideA > kSideB ? kSideA : kSideB;
 constexpr uint32_t kTmQ = 0, kTmS0 = 256, kTmS1 = 384;       // S-side TMEM columns
 constexpr uint32_t kFlagRescale = 2;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // deadline of every wait (wall clock)
+constexpr uint64_t kDrainNs = 2000000000ull;    // deadline of the exit drains
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
@@ -122,6 +124,9 @@ struct TcParams {
   int32_t tiles_per_seq, splits, chunk, n_items;
   const int4* info;  // per work item: sequence, split, tile, prefix length (longest first)
   float scale_log2;
+  uint64_t timeout_ns;        // deadline of every wait
+  int32_t test_skip_loads;    // testing hook: the S-side producer issues no key loads
+  int32_t* test_exit_counts;  // testing hook: [CTAs that left, CTAs that left aborted]
 };
 
 struct Shared {
@@ -132,6 +137,7 @@ struct Shared {
   uint64_t qr_full, q_free, pdst_free[kNInbox];
   uint64_t p_full[kNInbox];
   uint64_t drain, job_full, corr_done, epi_done, final_bar;
+  uint64_t timeout_ns;
   uint32_t tmem_base;
   volatile int abort;
   volatile int job_type, job_buf;
@@ -228,10 +234,35 @@ __device__ __noinline__ bool wait_bar_slow(Shared& sh, uint32_t a, uint32_t pari
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (sh.abort) return false;
-    if (globaltimer() - t0 > kTimeoutNs) {
+    if (globaltimer() - t0 > sh.timeout_ns) {
       raise_abort(sh, status, TV_ERR_TIMEOUT);
       return false;
     }
+  }
+}
+
+// Exit drain: wait for phase `parity` of a barrier that asynchronous work (a TMA load, the
+// tensor cores) still has to complete, whether or not the kernel is aborting, so that no
+// copy or MMA is in flight when the CTA frees its tensor memory and leaves.  Bounded by its
+// own deadline; if that runs out the kernel reports TV_ERR_TIMEOUT and leaves anyway.
+__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer() - t0 > kDrainNs) {
+      report(status, TV_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Drain a ring of n stages whose full barriers got `count` loads so far: the last issue of
+// each stage may still be in flight (earlier ones were consumed before it was re-armed).
+__device__ __noinline__ void drain_ring(uint64_t* full, uint32_t n, uint32_t count,
+                                        int32_t* status) {
+  for (uint32_t k = 0; k < n && k < count; ++k) {
+    const uint32_t u = count - 1 - k;
+    drain_wait(&full[u % n], (u / n) & 1, status);
   }
 }
 
@@ -330,6 +361,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
       // The refill latency of the rings is on the critical path: each cache layout gets its
       // own lean loop (the branch is taken once per tile).
       uint32_t u = 0, rc = 0, qi = 0;
+      auto produce = [&]() {
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         if (it.ns == 0) continue;
@@ -390,6 +422,13 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           tma_load_4d(rope + rs * kChunkS, ml + 1, 0, 0, 0, 0, &sh.rope_full[rs]);
         }
       }
+      };
+      if (!p.test_skip_loads) produce();
+      // leave no load in flight (after an abort the consumers stop taking stages; in a
+      // normal run these phases have completed already)
+      drain_ring(sh.slat_full, kNLS, u, p.status);
+      drain_ring(sh.rope_full, kNRope, rc, p.status);
+      drain_ring(&sh.qr_full, 1, qi, p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: S = Q K^T, 128 keys per step ----------------------
@@ -466,8 +505,9 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         mma_commit(&sh.q_free);
         ++qc;
       }
+      // every MMA and TMEM copy this thread issued completes before tensor memory is freed
       mma_commit(&sh.final_bar);
-      wait_bar(sh, &sh.final_bar, 0, p.status);
+      drain_wait(&sh.final_bar, 0, p.status);
     }
   } else if (warp >= 4) {
     // ---------------- softmax warpgroup: thread r owns tile row r ------------------
@@ -648,6 +688,7 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
     if (lane == 0) {
       prefetch_tensormap(map_lat);
       uint32_t u = 0;
+      auto produce = [&]() {
       for (int rr = 0, item; (item = item_at(p, rr, cid, ncl)) >= 0 && !sh.abort; ++rr) {
         const Item it = decode(p, item);
         // cache rows of each step's blocks are looked up a step ahead
@@ -677,6 +718,9 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
           }
         }
       }
+      };
+      produce();
+      drain_ring(sh.olat_full, kNLO, u, p.status);  // no load left in flight
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: O += P V ------------------------------------------
@@ -745,7 +789,7 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
       sh.job_type = 0;  // exit
       mbar_arrive(&sh.job_full);
       mma_commit(&sh.final_bar);
-      wait_bar(sh, &sh.final_bar, 0, p.status);
+      drain_wait(&sh.final_bar, 0, p.status);
     }
   } else if (warp >= 4) {
     // ---------------- rescale / epilogue warpgroup: thread r owns tile row r -------
@@ -862,6 +906,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
     mbar_init(&sh.epi_done, 128);
     mbar_init(&sh.final_bar, 1);
     sh.abort = 0;
+    sh.timeout_ns = p.timeout_ns;
     sh.job_type = 0;
     sh.job_buf = 0;
     if (rank == 1) {
@@ -892,6 +937,10 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap map_lat_s,
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(sh.tmem_base, 512);
+  if (p.test_exit_counts && threadIdx.x == 0) {
+    atomicAdd(p.test_exit_counts, 1);
+    if (sh.abort) atomicAdd(p.test_exit_counts + 1, 1);
+  }
   cluster_sync();  // neither CTA leaves while the other may still touch its memory
 }
 
@@ -1019,6 +1068,12 @@ prep_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, in
 }
 
 // ---- host side -----------------------------------------------------------------------
+// Testing hook (tv_testing_set_wait_fault): off unless a test turns it on.
+std::mutex g_test_mu;
+int g_test_skip_loads = 0;
+uint64_t g_test_deadline_ns = 0;
+int32_t* g_test_exit_counts = nullptr;
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 int g_max_clusters[64] = {};
@@ -1103,10 +1158,12 @@ int64_t gathered_seq_rows(const tv_attn_args* a) {
 }
 
 // Paged cache: gather it into a contiguous view (true) or use per-step tensor maps (false).
+// The caller may force either form (tv_paged_view); AUTO gathers above 64 MB of keys.
 bool use_gather(const tv_attn_args* a) {
-  if (!a->cache.page_table) return false;
+  if (!a->cache.page_table || a->paged_view == TV_PAGED_STEP_MAPS) return false;
   const int64_t rows = (int64_t)a->B * gathered_seq_rows(a);
-  return rows < (1ll << 31) && rows * (kDL + kDR) * 2 > (64ll << 20);
+  if (rows >= (1ll << 31)) return false;
+  return a->paged_view == TV_PAGED_GATHER || rows * (kDL + kDR) * 2 > (64ll << 20);
 }
 
 // 128-key steps of the longest sequence (per-step tensor maps of a paged cache).
@@ -1306,6 +1363,13 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.max_pages = a->cache.max_pages;
   p.paged = paged ? 1 : 0;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+  p.timeout_ns = kTimeoutNs;
+  {
+    std::lock_guard<std::mutex> lock(g_test_mu);
+    p.test_skip_loads = g_test_skip_loads;
+    if (g_test_deadline_ns) p.timeout_ns = g_test_deadline_ns;
+    p.test_exit_counts = g_test_exit_counts;
+  }
   if (p.n_items == 0) return cudaSuccess;
 
   {
@@ -1352,3 +1416,13 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
 }
 
 }  // namespace tv
+
+extern "C" int tv_testing_set_wait_fault(int skip_key_loads, uint64_t deadline_ns,
+                                         int32_t* exit_counts) {
+  if (skip_key_loads < 0 || skip_key_loads > 1) return TV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(tv::g_test_mu);
+  tv::g_test_skip_loads = skip_key_loads;
+  tv::g_test_deadline_ns = deadline_ns;
+  tv::g_test_exit_counts = exit_counts;
+  return TV_OK;
+}

@@ -69,8 +69,9 @@ int check_attn(const tv_attn_args* a) {
   } else if (a->cache.kv_stride_b < kv_max) {
     return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: kv_stride_b < max_prefix_len + Q%s");
   }
-  if (a->path < TV_PATH_AUTO || a->path > TV_PATH_TCGEN05 || a->num_splits < 0)
-    return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: bad path or num_splits%s");
+  if (a->path < TV_PATH_AUTO || a->path > TV_PATH_TCGEN05 || a->num_splits < 0 ||
+      a->paged_view < TV_PAGED_AUTO || a->paged_view > TV_PAGED_GATHER)
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: bad path, num_splits or paged_view%s");
   return TV_OK;
 }
 

@@ -15,7 +15,9 @@
 // earlier call are never read.  Calls share the one array: two calls whose kernels can
 // overlap on the GPU (different streams without ordering, or different host threads)
 // race on it and must be serialised by the caller.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdio>
 #include <mutex>
@@ -34,33 +36,58 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// The address is cached per device together with the CUDA context it was looked up in: a
+// new context on the device (after cudaDeviceReset, or a context the caller made current)
+// loads the module again, possibly elsewhere, so the lookup is then repeated.
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
 
-// Device address of the scratch array on the current device; looked up once per device
-// (the first call on a device does it, so that call should come before any stream
-// capture).  Returns nullptr and sets the error text on failure.
+CUcontext current_context() {
+  std::call_once(g_ctx_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  CUcontext c = nullptr;
+  if (!g_ctx_current || g_ctx_current(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+void set_error(const char* what, cudaError_t e) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "tv_verify_attn_noalloc: %s failed: %s", what, cudaGetErrorString(e));
+  tv::set_last_error(buf);
+}
+
+// Device address of the scratch array in the current device's current context.  The first
+// call on a device (and the first after that device's context changed) looks it up with
+// cudaGetSymbolAddress, which may load the library's device code; make that call before
+// any stream capture.  Returns nullptr and sets the error text on failure.
 void* scratch_for_current_device() {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    char buf[256];
-    snprintf(buf, sizeof(buf), "tv_verify_attn_noalloc: cudaGetDevice failed: %s",
-             cudaGetErrorString(e));
-    tv::set_last_error(buf);
+    set_error("cudaGetDevice", e);
     return nullptr;
   }
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
-      char buf[256];
-      snprintf(buf, sizeof(buf), "tv_verify_attn_noalloc: cudaGetSymbolAddress failed: %s",
-               cudaGetErrorString(e));
-      tv::set_last_error(buf);
+      set_error("cudaGetSymbolAddress", e);
+      g_scratch_ptr[dev] = nullptr;
       return nullptr;
     }
     g_scratch_ptr[dev] = p;
+    // the look-up makes the runtime's context current if there was none yet
+    g_scratch_ctx[dev] = ctx ? ctx : current_context();
   }
   return g_scratch_ptr[dev];
 }
@@ -95,11 +122,11 @@ int tv_verify_attn_noalloc(const tv_attn_args* a, void* stream) {
     tv::set_last_error(buf);
     return TV_ERR_WORKSPACE;
   }
-  void* ws = nullptr;
-  if (need > 0) {
-    ws = scratch_for_current_device();
-    if (!ws) return TV_ERR_CUDA;
-  }
+  // The address is resolved on every call, also when this request needs no scratch, so
+  // that the first call on a device always does the one-time look-up.
+  void* scratch = scratch_for_current_device();
+  if (!scratch) return TV_ERR_CUDA;
+  void* ws = need > 0 ? scratch : nullptr;
   cudaError_t e = tv::launch_attn_simt(a, plan, ws, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     char buf[256];

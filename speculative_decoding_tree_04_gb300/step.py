@@ -35,11 +35,13 @@ class VerifyStep:
     HOST_KEYS = ("parent", "prefix_len", "page_table", "q_latent", "q_pe", "kpe_tree",
                  "c_kv", "k_pe")
 
-    def __init__(self, inp: dict, device="cuda", path=tv.PATH_AUTO, num_splits=0):
+    def __init__(self, inp: dict, device="cuda", path=tv.PATH_AUTO, num_splits=0,
+                 paged_view=tv.PAGED_AUTO):
         self.inp = inp
         self.device = torch.device(device)
         self.path = path
         self.num_splits = num_splits
+        self.paged_view = paged_view
         d = self.device
         B, Q, H, DL = inp["B"], inp["Q"], inp["H"], inp["DL"]
         self.B, self.Q, self.H, self.DL, self.DR = B, Q, H, DL, inp["DR"]
@@ -67,7 +69,7 @@ class VerifyStep:
         return tv.attn_args(self.q_latent, self.q_pe, self.c_kv, self.k_pe, self.prefix_len,
                             self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
                             self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
-                            self.status, self.path, self.num_splits)
+                            self.status, self.path, self.num_splits, self.paged_view)
 
     def _alloc_workspace(self):
         need = tv.workspace_size(self.attn_args())
@@ -95,7 +97,7 @@ class VerifyStep:
                        self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
                        self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
                        self.status, self.path, self.num_splits, workspace=self.workspace,
-                       stream=stream)
+                       stream=stream, paged_view=self.paged_view)
 
     def run(self, stream=None):
         self.visibility(stream)

@@ -81,8 +81,8 @@ def generate(name: str | None = None, seed: int | None = None, **kw) -> dict:
     """Draw one verify step's raw inputs.
 
     ``name`` picks a workload from WORKLOADS; keyword arguments override its fields (B, H,
-    Q, DL, DR, prefix=(lo, hi), tree, dtype "fp32"|"bf16", q_var, scale_den, paged, page
-    size ``page``).  Returns a dict of numpy arrays plus the sizes:
+    Q, DL, DR, prefix=(lo, hi), tree, dtype "fp32"|"bf16", q_var, q_pe_var (rope part of
+    the queries; defaults to q_var), scale_den, paged, page size ``page``).  Returns a dict of numpy arrays plus the sizes:
 
       parent [B,Q] int32, prefix_len [B] int32,
       q_latent [B,Q,H,DL], q_pe [B,Q,H,DR] (un-rotated), kpe_tree [B,Q,DR] (un-rotated)
@@ -115,8 +115,10 @@ def generate(name: str | None = None, seed: int | None = None, **kw) -> dict:
     kv_len = prefix_len.astype(np.int64) + Q
 
     qstd = 1.0 / math.sqrt(cfg["q_var"])
+    # q_pe_var (optional) gives the rope part of the queries its own variance 1/q_pe_var
+    pstd = 1.0 / math.sqrt(cfg.get("q_pe_var", cfg["q_var"]))
     q_latent = (r_q.standard_normal((B, Q, H, DL), dtype=np.float32) * np.float32(qstd))
-    q_pe = (r_qpe.standard_normal((B, Q, H, DR), dtype=np.float32) * np.float32(qstd))
+    q_pe = (r_qpe.standard_normal((B, Q, H, DR), dtype=np.float32) * np.float32(pstd))
     kpe_tree = r_kt.standard_normal((B, Q, DR), dtype=np.float32)
 
     if cfg["paged"]:

@@ -25,6 +25,7 @@ TV_OK, TV_ERR_INVALID_ARG, TV_ERR_INVALID_TREE, TV_ERR_UNSUPPORTED = 0, -1, -2, 
 TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_ERR_WORKSPACE, TV_ERR_BOUNDS = -4, -5, -6, -7
 TV_F32, TV_BF16 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TCGEN05 = 0, 1, 2
+PAGED_AUTO, PAGED_STEP_MAPS, PAGED_GATHER = 0, 1, 2
 
 
 class TVError(RuntimeError):
@@ -57,6 +58,7 @@ class AttnArgs(ctypes.Structure):
         ("status", ctypes.c_void_p),
         ("path", ctypes.c_int32),
         ("num_splits", ctypes.c_int32),
+        ("paged_view", ctypes.c_int32),
     ]
 
 
@@ -87,16 +89,23 @@ def load():
     lib.tv_status_string.restype = ctypes.c_char_p
     lib.tv_last_error.restype = ctypes.c_char_p
     lib.tv_version.restype = ctypes.c_int
+    lib.tv_testing_set_wait_fault.argtypes = [i32, ctypes.c_uint64, P]
     _lib = lib
     return lib
 
 
-def header_functions(path: str = HEADER):
-    """Names of the functions include/tv.h declares (for symbol checks)."""
-    with open(path) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tv_\w+)\s*\(", text, re.M)))
+def header_functions(paths=None):
+    """Names of the functions the headers under include/ declare (for symbol checks)."""
+    if paths is None:
+        inc = os.path.dirname(HEADER)
+        paths = sorted(os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h"))
+    names = set()
+    for path in ([paths] if isinstance(paths, str) else paths):
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tv_\w+)\s*\(", text, re.M))
+    return sorted(names)
 
 
 def _check(rc, what):
@@ -182,7 +191,7 @@ def rope_neox(x, out, prefix_len, depth, base=10000.0, cache: CacheLayout | None
 
 def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
               page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
-              num_splits=0) -> AttnArgs:
+              num_splits=0, paged_view=PAGED_AUTO) -> AttnArgs:
     _need_cuda(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, page_table, status)
     B, Q, H, DL = q_latent.shape
     DR = q_pe.shape[-1]
@@ -206,7 +215,7 @@ def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_
     a.anc = anc.data_ptr()
     a.out, a.lse = out.data_ptr(), lse.data_ptr()
     a.status = None if status is None else status.data_ptr()
-    a.path, a.num_splits = int(path), int(num_splits)
+    a.path, a.num_splits, a.paged_view = int(path), int(num_splits), int(paged_view)
     return a
 
 
@@ -245,13 +254,14 @@ def noalloc_scratch_bytes() -> int:
 
 def verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
                 page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
-                num_splits=0, workspace=None, stream=None):
+                num_splits=0, workspace=None, stream=None, paged_view=PAGED_AUTO):
     """Tree-verify attention; out [B,Q,H,DL] and lse [B,Q,H] (float32) are written.
 
     ``workspace`` (a CUDA uint8 tensor) is allocated through torch and cached per device
     when not given."""
     a = attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale,
-                  max_prefix_len, page_table, page_size, kv_stride_b, status, path, num_splits)
+                  max_prefix_len, page_table, page_size, kv_stride_b, status, path, num_splits,
+                  paged_view)
     need = workspace_size(a)
     if workspace is None and need > 0:
         key = q_latent.device

@@ -20,7 +20,8 @@ from speculative_decoding_tree_04_gb300 import tv
 FAKE = 1 << 20  # placeholder device address; planning never dereferences it
 
 
-def args(B, H, Q, max_prefix, paged=False, dt=tv.TV_BF16, num_splits=0, path=tv.PATH_AUTO):
+def args(B, H, Q, max_prefix, paged=False, dt=tv.TV_BF16, num_splits=0, path=tv.PATH_AUTO,
+         paged_view=tv.PAGED_AUTO):
     a = tv.AttnArgs()
     a.struct_size = ctypes.sizeof(tv.AttnArgs)
     a.B, a.H, a.Q, a.d_latent, a.d_rope = B, H, Q, 512, 64
@@ -37,6 +38,7 @@ def args(B, H, Q, max_prefix, paged=False, dt=tv.TV_BF16, num_splits=0, path=tv.
     a.max_prefix_len = max_prefix
     a.num_splits = num_splits
     a.path = path
+    a.paged_view = paged_view
     return a
 
 
@@ -111,3 +113,20 @@ def test_call_refuses_a_bad_workspace_before_launching(tvlib, offset, short):
     rc = lib().tv_verify_attn(ctypes.byref(a), ctypes.c_void_p(FAKE + offset), ws_bytes, None)
     assert rc == tv.TV_ERR_WORKSPACE
     assert lib().tv_last_error()
+
+
+def test_paged_view_forces_either_form(tvlib):
+    # small paged cache: per-step maps by default, the gathered key view when forced
+    small = dict(B=8, H=64, Q=9, max_prefix=4096, paged=True, num_splits=1)
+    assert launches(args(**small)) == 2
+    assert launches(args(**small, paged_view=tv.PAGED_GATHER)) == 3
+    assert workspace(args(**small, paged_view=tv.PAGED_GATHER)) >= 8 * 4224 * (512 + 64) * 2
+    # large paged cache: gathered by default, per-step maps when forced
+    big = dict(B=32, H=64, Q=33, max_prefix=8192, paged=True)
+    assert launches(args(**big)) == 3
+    assert launches(args(**big, paged_view=tv.PAGED_STEP_MAPS)) == 2
+    assert workspace(args(**big, paged_view=tv.PAGED_STEP_MAPS)) < 32 * 8225 * 1152
+    # a contiguous cache ignores the setting
+    assert launches(args(32, 64, 33, 8192, paged_view=tv.PAGED_GATHER)) == 2
+    # out-of-range values are argument errors
+    assert path(args(**small, paged_view=3)) == tv.TV_ERR_INVALID_ARG

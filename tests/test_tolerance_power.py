@@ -1,0 +1,52 @@
+"""The bf16 parity rule can fail (CPU only, the oracle against variants of itself).
+
+the benchmark spec's bf16 bound, max_abs <= 2e-2, is about as large as the outputs of a softmax
+over thousands of keys, so on its own it cannot tell a correct kernel from one that drops
+a term.  tests/compare.py adds a per-row rule derived from the arithmetic (relative rms
+<= 2^-7).  Here the oracle computes two plausible kernel mistakes on two sequences of the
+B8 H64 Q9 paged workload (prefixes of 1024..4096 keys):
+  * the rope term q_pe.k_pe left out of the scores;
+  * one 64-key page of the gathered key view taken from the wrong cache page;
+and each must fail the derived rule while still passing max_abs <= 2e-2 (which is why the
+stricter rule is needed).  The correct oracle output passes against itself trivially.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_tree_04_gb300 import synth
+from tests.compare import BF16_ABS, BF16_ROW_RMS, errors
+
+
+@pytest.fixture(scope="module")
+def case():
+    inp = synth.generate("cfg4_bf16", B=2)
+    ref = oracle.tree_verify_step(inp)
+    return inp, ref
+
+
+def _attn(inp, ref, q_pe=None, page_table=None):
+    vis = ref["vis"]
+    return oracle.verify_attn(inp["q_latent"], ref["q_pe_rot"] if q_pe is None else q_pe,
+                              inp["c_kv"], ref["k_pe_cache"], inp["prefix_len"], vis,
+                              inp["scale"], inp["page_table"] if page_table is None else page_table,
+                              inp["page_size"], inp["kv_stride_b"])
+
+
+def test_dropped_rope_term_fails_the_derived_rule(case):
+    inp, ref = case
+    out, _ = _attn(inp, ref, q_pe=np.zeros_like(ref["q_pe_rot"]))
+    e = errors(out, ref["out"], inp["DL"])
+    assert e["max_abs"] <= BF16_ABS            # the loose bound alone would pass it
+    assert e["row_rms"] > 3 * BF16_ROW_RMS, e
+
+
+def test_one_wrong_page_fails_the_derived_rule(case):
+    inp, ref = case
+    pt = inp["page_table"].copy()
+    # page 5 of sequence 1 (a prefix page) read from another sequence's page
+    pt[1, 5] = inp["page_table"][0, 7]
+    out, _ = _attn(inp, ref, page_table=pt)
+    e = errors(out[1], ref["out"][1], inp["DL"])
+    assert e["max_abs"] <= BF16_ABS
+    assert e["row_rms"] > 3 * BF16_ROW_RMS, e

@@ -329,6 +329,68 @@ def time_steps(step, steps, warmup, eager, flush, dev, barrier, cold=True):
     return ms, ams, graphs
 
 
+def time_post_verify(args, inp, dev, flush, barrier, peaks, pg):
+    """Time tv_tree_accept (argmax of every node's logits + the greedy walk) and
+    tv_compact_kv on the workload's trees with a 163840-token float32 vocabulary: HBM-bound
+    (the logits are read once)."""
+    import torch
+    from speculative_decoding_tree_04_gb300 import synth, tv
+    from speculative_decoding_tree_04_gb300.step import VerifyStep
+    B, Q = inp["B"], inp["Q"]
+    acc = synth.generate_accept(inp, ties=False)
+    logits = torch.from_numpy(acc["logits"]).to(dev)
+    del acc["logits"]
+    parent = torch.from_numpy(inp["parent"]).to(dev)
+    tokens = torch.from_numpy(acc["tokens"]).to(dev)
+    a = torch.zeros(B, dtype=torch.int32, device=dev)
+    path = torch.zeros((B, Q), dtype=torch.int32, device=dev)
+    emit = torch.zeros((B, Q), dtype=torch.int32, device=dev)
+    newp = torch.zeros(B, dtype=torch.int32, device=dev)
+    step = VerifyStep(inp, device=dev)
+    step.run()
+    cache = tv.make_cache(step.page_table, inp["page_size"], inp["kv_stride_b"],
+                          min(step.c_kv.shape[0], step.k_pe.shape[0]))
+    ws = torch.empty(tv.accept_workspace_size(B, Q, acc["vocab"]), dtype=torch.uint8, device=dev)
+
+    def once():
+        tv.tree_accept(logits, parent, tokens, a, path, emit, workspace=ws)
+
+    def compact():
+        tv.compact_kv(step.c_kv, step.k_pe, cache, step.prefix_len, path, a, newp)
+
+    for _ in range(args.warmup):
+        once()
+        compact()
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.add_(1.0)
+        ev[k][0].record()
+        once()
+        ev[k][1].record()
+        compact()
+        ev[k][2].record()
+    barrier()
+    acc_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    cmp_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    acc_ms, cmp_ms = max_over_ranks([acc_ms, cmp_ms], pg, dev)
+    nbytes = logits.numel() * logits.element_size()
+    gbs = nbytes / (acc_ms * 1e-3) / 1e9
+    moved = int(a.sum().item())
+    res = {"workload": f"{args.workload} trees, {acc['vocab']}-token float32 logits "
+                       f"({nbytes / 1e6:.0f} MB), accepted nodes moved in the paged cache",
+           "accept_ms": acc_ms, "compact_ms": cmp_ms, "ms": acc_ms + cmp_ms,
+           "accepted_tokens": moved,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                        "peak_source": peaks["source"] + " copy bandwidth (MEASURED_PEAKS hbm_gbs)",
+                        "algorithmic_bytes": nbytes, "traffic": None},
+           "launches_per_step": 3}
+    del logits, step
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,6 +543,11 @@ def main():
         del st2
         torch.cuda.empty_cache()
 
+    # ---- post-verify: greedy tree acceptance + KV compaction on the same trees -------
+    post = None
+    if args.workload in ("cfg5_bf16", "cfg4_bf16") and args.batch == 0:
+        post = time_post_verify(args, inp, dev, flush, barrier, peaks, pg)
+
     if rank != 0:
         pg.destroy_process_group() if pg is not None else None
         return
@@ -526,6 +593,7 @@ def main():
         "attn_ms_warm_l2": ams_warm,
         "roofline": roof,
         "configs": configs,
+        "post_verify": post,
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

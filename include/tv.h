@@ -71,6 +71,16 @@ typedef enum { TV_PATH_AUTO = 0, TV_PATH_SIMT = 1, TV_PATH_TCGEN05 = 2 } tv_path
  * TV_PAGED_GATHER needs B * (max_prefix_len + Q rounded up to 128) < 2^31 rows. */
 typedef enum { TV_PAGED_AUTO = 0, TV_PAGED_STEP_MAPS = 1, TV_PAGED_GATHER = 2 } tv_paged_view;
 
+/* Which keys a query row sees (tv_attn_args.mask_mode).  [GOLDEN] §"Principled
+ * Abstraction": one forward_tokens call serves tree verification, autoregressive decoding
+ * (one query, every key) and prefill (causal masking).
+ *   TV_MASK_TREE   : node i sees the P prefix keys and its ancestor-or-self tree keys
+ *                    (anc bitsets from tv_build_visibility; Q <= 64);
+ *   TV_MASK_CAUSAL : query token i (at logical key P + i) sees keys 0 .. P + i: prefill of
+ *                    Q tokens after a cache of P (P = 0: no prior cache); anc is not read
+ *                    and may be NULL; Q is limited only by B*Q*H < 2^31. */
+typedef enum { TV_MASK_TREE = 0, TV_MASK_CAUSAL = 1 } tv_mask_mode;
+
 /*
  * Geometry of the latent KV cache.  Logical key j (0 <= j < prefix_len[b] + Q) of
  * sequence b lives in cache row
@@ -137,7 +147,8 @@ int tv_build_visibility(const int32_t* parent, int B, int Q, uint64_t* anc, int3
  *       allowed (in place).
  * in_dt / out_dt : TV_F32 or TV_BF16 each.
  * prefix_len [B], depth [B, Q]: device int32 (depth from tv_build_visibility; a negative
- *       depth -- an invalid tree -- leaves that row untouched).  With out_cache, rows whose
+ *       depth -- an invalid tree -- leaves that row untouched).  depth may be NULL: then
+ *       row i is at position prefix_len[b] + i (a chain of tokens, as in prefill).  With out_cache, rows whose
  *       slot lies outside the geometry (negative prefix_len, a page index >= max_pages, a
  *       negative page-table entry, or a slot >= kv_stride_b) are skipped.
  * Returns TV_ERR_INVALID_ARG for odd or non-positive d_rope, n_heads < 1, or strides
@@ -158,6 +169,8 @@ int tv_rope_neox(const void* in, tv_dtype in_dt, int64_t in_stride_row,
  *     s_j = scale * ( q_latent[b,i,h,:] . c_kv[j,:]  +  q_pe[b,i,h,:] . k_pe[j,:] )
  * over the visible keys V = { j < P_b } U { P_b + k : bit k of anc[b*Q+i] }, and
  *     out[b,i,h,:] = sum_{j in V} softmax(s)_j * c_kv[j,:],   lse[b,i,h] = ln sum exp(s_j).
+ * With mask_mode = TV_MASK_CAUSAL the visible set is V = { j <= P_b + i } instead (prefill;
+ * Q > 64 allowed, anc unused).
  */
 typedef struct {
   uint32_t struct_size;     /* sizeof(tv_attn_args): ABI check */
@@ -180,6 +193,7 @@ typedef struct {
   int32_t path;             /* tv_path; TV_PATH_AUTO normally */
   int32_t num_splits;       /* 0 = automatic; else force this many KV splits */
   int32_t paged_view;       /* tv_paged_view; TV_PAGED_AUTO normally */
+  int32_t mask_mode;        /* tv_mask_mode; TV_MASK_TREE for tree verification */
 } tv_attn_args;
 
 /* Bytes of workspace tv_verify_attn needs for these arguments (0 if none).  The size
@@ -241,6 +255,72 @@ int tv_verify_attn_noalloc(const tv_attn_args* a, void* stream);
 
 /* Size in bytes of the fixed scratch array behind tv_verify_attn_noalloc. */
 size_t tv_noalloc_scratch_bytes(void);
+
+/*
+ * tv_tree_accept -- greedy acceptance of a verified draft tree.
+ *
+ * [RoPE] §"The Broader Context: A Full Native Engine from Scratch" names a greedy
+ * tree-accept kernel in the DDTree decode loop, whose greedy output must equal greedy
+ * autoregressive decoding token for token; [GOLDEN] §"Context: The Quest for a
+ * Hyper-Optimized Inference Stack" lists it among the engine's three custom kernels.  The
+ * pages give no formula; the reading taken here:
+ *   target[b,i] = argmax_v logits[b,i,v]  (the target model's next token after node i;
+ *                 ties go to the smallest token id; logits must be finite),
+ *   walk from the root: the next accepted node is the child c of the current node with
+ *   tokens[b,c] == target[b,current] (the smallest such c), until there is none; the
+ *   bonus token is target[b,last accepted node].
+ *
+ * logits     : device [B, Q, vocab] (row (b,i) at logits + (b*Q+i)*logits_row_stride
+ *              elements), F32 or BF16 (rows at 16-byte boundaries stream fastest).
+ * parent     : device [B, Q] int32 draft tree (as for tv_build_visibility).
+ * tokens     : device [B, Q] int32 draft token of every node (node 0's entry, the root
+ *              token, is not read).
+ * target     : device [B, Q] int32 out, nullable: the argmax of every node's logits.
+ * accept_len : device [B] int32 out: accepted draft nodes A (0 .. Q-1).
+ * path       : device [B, Q] int32 out: 0 (the root), then the accepted nodes in depth
+ *              order, then -1.
+ * new_tokens : device [B, Q] int32 out: the accepted draft tokens, then the bonus token,
+ *              then -1 (A + 1 tokens emitted by the step).
+ * status     : see the conventions.  A sequence with an invalid parent array gets A = 0,
+ *              path = [0, -1, ...], new_tokens all -1 and TV_ERR_INVALID_TREE.
+ * workspace  : device memory of tv_tree_accept_workspace_size(B, Q, vocab) bytes, 256-byte
+ *              aligned (the per-chunk argmax keys); scratch, reusable after the call.
+ * Returns TV_ERR_UNSUPPORTED for Q > 64, TV_ERR_INVALID_ARG for bad sizes or pointers,
+ * TV_ERR_WORKSPACE for a missing, misaligned or short workspace.
+ */
+size_t tv_tree_accept_workspace_size(int B, int Q, int64_t vocab);
+int tv_tree_accept(const void* logits, tv_dtype logits_dt, int64_t vocab,
+                   int64_t logits_row_stride, const int32_t* parent, const int32_t* tokens,
+                   int B, int Q, int32_t* target, int32_t* accept_len, int32_t* path,
+                   int32_t* new_tokens, int32_t* status, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/*
+ * tv_compact_kv -- post-verify compaction of the latent KV cache.
+ *
+ * [RoPE] §"The Broader Context: A Full Native Engine from Scratch": the engine keeps a KV
+ * cache with post-verify compaction.  Reading taken here: node i's row sits at logical key
+ * prefix_len[b] + i; after acceptance the node at depth d (path[b, d], from tv_tree_accept)
+ * moves to logical key prefix_len[b] + d, for d = 1 .. accept_len[b] (the root stays), so
+ * that the accepted tokens follow the prefix contiguously.  Both the c_kv row and the k_pe
+ * row move; the k_pe row was rotated at position prefix_len + depth, which is its new key
+ * index, so it moves unchanged.  new_prefix_len[b] = prefix_len[b] + 1 + accept_len[b].
+ *
+ * c_kv, k_pe : device cache arrays (rows of d_latent / d_rope elements at the given row
+ *              strides, in elements); row sizes, strides and pointers must be multiples of
+ *              16 bytes.  Updated in place.
+ * cache      : host struct, the cache geometry (page table or contiguous) with num_rows > 0.
+ * prefix_len [B], path [B, Q], accept_len [B]: device int32 (path and accept_len as written
+ *              by tv_tree_accept).  new_prefix_len [B]: device int32 out (may alias
+ *              prefix_len only if the caller does not need the old value).
+ * status     : a sequence whose path or keys fall outside the geometry is left unmoved,
+ *              keeps new_prefix_len = prefix_len and gets TV_ERR_BOUNDS.
+ */
+int tv_compact_kv(void* c_kv, void* k_pe, tv_dtype kv_dt, int64_t ckv_row_stride,
+                  int64_t kpe_row_stride, int d_latent, int d_rope,
+                  const tv_cache_layout* cache, const int32_t* prefix_len, const int32_t* path,
+                  const int32_t* accept_len, int B, int Q, int32_t* new_prefix_len,
+                  int32_t* status, void* stream);
 
 /* Text for a tv_status code (static storage). */
 const char* tv_status_string(int code);

@@ -48,6 +48,7 @@ struct SimtArgs {
   int32_t* status;
   int B, H, Q, DL, DR, max_prefix;
   int splits, chunk, head_blocks;
+  int causal;  // TV_MASK_CAUSAL: row i sees keys 0 .. P + i
   float scale_log2;
 };
 
@@ -139,8 +140,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(const SimtArgs a
       bad = kv_len > a.cache.kv_stride_b;
   }
   const int64_t k0 = (int64_t)s * a.chunk;
-  const int64_t k1 = bad ? k0 : (k0 + a.chunk < kv_len ? k0 + a.chunk : kv_len);
-  const uint64_t anc = a.anc[(int64_t)b * a.Q + i];
+  // causal rows see keys up to their own (P + i); tree rows up to the last tree key
+  const int64_t k_end = a.causal ? (int64_t)P + i + 1 : kv_len;
+  const int64_t k1 = bad ? k0 : (k0 + a.chunk < k_end ? k0 + a.chunk : k_end);
+  const uint64_t anc = a.causal ? 0ull : a.anc[(int64_t)b * a.Q + i];
+  // every key below pvis is visible (the prefix; for causal rows all keys up to P + i)
+  const int64_t pvis = a.causal ? k_end : (int64_t)P;
   if (bad && threadIdx.x == 0 && s == 0 && hb == 0 && i == 0) report(a.status, TV_ERR_BOUNDS);
 
   // Query rows of this warp in registers: chunk c = lane + 32 t covers elements 4c..4c+3
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(const SimtArgs a
     const T* tile = tiles + buf * kTileKeys * E;
     const int64_t base = k0 + (int64_t)t * kTileKeys;
     const int64_t j = base + lane;
-    const bool vis = j < k1 && (j < P || ((anc >> (int)(j - P)) & 1ull));
+    const bool vis = j < k1 && (j < pvis || (!a.causal && ((anc >> (int)(j - P)) & 1ull)));
     const unsigned vm = __ballot_sync(0xffffffffu, vis);
     if (warp_live && vm) {
       // ---- scores of the visible keys (log2 domain) ----
@@ -479,6 +484,7 @@ cudaError_t launch_attn_simt(const tv_attn_args* a, const SimtPlan& p, void* ws,
   sa.chunk = p.chunk;
   sa.head_blocks = p.head_blocks;
   sa.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
+  sa.causal = a->mask_mode == TV_MASK_CAUSAL ? 1 : 0;
   const size_t rows = (size_t)a->B * a->Q * a->H;
   sa.ws_out = (float*)ws;
   sa.ws_lse = ws ? (float*)((char*)ws + ((size_t)p.splits * rows * a->d_latent * 4 + 255) /

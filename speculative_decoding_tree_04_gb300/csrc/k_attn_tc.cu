@@ -125,6 +125,7 @@ struct TcParams {
   const int4* info;  // per work item: sequence, split, tile, prefix length (longest first)
   float scale_log2;
   uint64_t timeout_ns;        // deadline of every wait
+  int32_t causal;             // TV_MASK_CAUSAL: row (node i, head) sees keys 0 .. P + i
   int32_t test_skip_loads;    // testing hook: the S-side producer issues no key loads
   int32_t* test_exit_counts;  // testing hook: [CTAs that left, CTAs that left aborted]
 };
@@ -167,7 +168,13 @@ __device__ __noinline__ Item decode_info(const TcParams& p, int4 v) {
   const int64_t kv_len = (int64_t)it.P + p.Q;
   it.bad = it.P < 0 || it.P > p.max_prefix || kv_len > p.seq_cap;
   it.k0 = (int64_t)it.s * p.chunk;
-  int64_t k1 = it.k0 + p.chunk < kv_len ? it.k0 + p.chunk : kv_len;
+  int64_t kend = kv_len;
+  if (p.causal) {
+    // no row of the tile sees past its last row's node
+    const int64_t hi = ((int64_t)(it.t + 1) * kRows - 1) / p.H;
+    kend = (int64_t)it.P + (hi < p.Q - 1 ? hi : p.Q - 1) + 1;
+  }
+  int64_t k1 = it.k0 + p.chunk < kend ? it.k0 + p.chunk : kend;
   if (it.bad) k1 = it.k0;
   it.nb = k1 > it.k0 ? (int)((k1 - it.k0 + kBN - 1) / kBN) : 0;
   it.ns = (it.nb + 1) >> 1;
@@ -544,7 +551,10 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         if (vrow) *lse_dst = -INFINITY;
         continue;
       }
-      const uint64_t anc = vrow ? p.anc[(int64_t)it.b * p.Q + trow / p.H] : 0ull;
+      const int node = trow / p.H;
+      const uint64_t anc = (vrow && !p.causal) ? p.anc[(int64_t)it.b * p.Q + node] : 0ull;
+      // every key below pv is visible: the prefix, or for a causal row all keys up to its own
+      const int64_t pv = p.causal ? (int64_t)it.P + node + 1 : (int64_t)it.P;
       const int64_t kv_end = (int64_t)it.P + p.Q;
       const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
 
@@ -596,11 +606,11 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         const bool two = 2 * st + 1 < it.nb;
         const int64_t key0 = it.k0 + (int64_t)st * kStep;
         const uint64_t vis0 =
-            (key0 + kBN > it.P || key0 + kBN > k1) ? block_vis(key0, it.P, k1, anc) : ~0ull;
+            (key0 + kBN > pv || key0 + kBN > k1) ? block_vis(key0, pv, k1, anc) : ~0ull;
         const uint64_t vis1 =
             !two ? 0ull
-                 : ((key0 + 2 * kBN > it.P || key0 + 2 * kBN > k1)
-                        ? block_vis(key0 + kBN, it.P, k1, anc)
+                 : ((key0 + 2 * kBN > pv || key0 + 2 * kBN > k1)
+                        ? block_vis(key0 + kBN, pv, k1, anc)
                         : ~0ull);
         apply_mask(t, vis0);
         apply_mask(t + 64, vis1);
@@ -996,7 +1006,7 @@ prep_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, in
             const unsigned char* ckv, int64_t ckv_page_bytes, const unsigned char* kpe,
             int64_t kpe_page_bytes, const int32_t* __restrict__ page_table, int max_pages,
             int64_t num_pages, int steps_per_seq, CUtensorMap* __restrict__ maps,
-            uint8_t* __restrict__ swap, int32_t* status) {
+            uint8_t* __restrict__ swap, int causal, int32_t* status) {
   griddep_launch_dependents();  // the attention kernel may start its set-up now
   if (blockIdx.x > 0) {
     const int64_t idx = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
@@ -1058,12 +1068,21 @@ prep_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, in
     order[rank] = i;
   }
   __syncthreads();
-  // item k: tile k % tiles of pair order[k / tiles]
+  // tree mask: item k is tile k % tiles of pair order[k / tiles] (all tiles of a pair
+  // cost the same); causal mask: a tile's keys end at its last row, so items go tile by
+  // tile from the last (longest) tile down, the pairs of each tile longest first
   for (int k = threadIdx.x; k < n_items; k += blockDim.x) {
-    const int q = k / tiles;
+    int q, t;
+    if (causal) {
+      q = k % n;
+      t = tiles - 1 - k / n;
+    } else {
+      q = k / tiles;
+      t = k - q * tiles;
+    }
     const int pair = ranked ? order[q] : q;
     const int b = pair / splits;
-    info[k] = make_int4(b, pair - b * splits, k - q * tiles, prefix_len[b]);
+    info[k] = make_int4(b, pair - b * splits, t, prefix_len[b]);
   }
 }
 
@@ -1364,6 +1383,7 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.paged = paged ? 1 : 0;
   p.scale_log2 = (float)((double)a->scale * 1.4426950408889634);
   p.timeout_ns = kTimeoutNs;
+  p.causal = a->mask_mode == TV_MASK_CAUSAL ? 1 : 0;
   {
     std::lock_guard<std::mutex> lock(g_test_mu);
     p.test_skip_loads = g_test_skip_loads;
@@ -1379,7 +1399,7 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
         pl.tiles_per_seq, pl.n_items, info, t_lat, t_rope, (const unsigned char*)a->c_kv,
         (int64_t)lat_row_bytes * kBN, (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN,
         a->cache.page_table, a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps, maps,
-        swap, a->status);
+        swap, a->mask_mode == TV_MASK_CAUSAL ? 1 : 0, a->status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

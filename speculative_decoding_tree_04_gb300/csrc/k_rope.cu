@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(128) rope_kernel(const Tin* in, int64_t isr, i
   const int64_t r = blockIdx.x;  // b*Q + i
   const int b = (int)(r / Q);
   const int i = (int)(r % Q);
-  const int dep = depth[r];
+  const int dep = depth ? depth[r] : i;  // no depth array: a chain, position P + i
   if (dep < 0) return;  // invalid tree: leave the row alone
   const int P = prefix_len[b];
   const int half = D / 2;

@@ -43,14 +43,20 @@ int check_attn(const tv_attn_args* a) {
     return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: struct_size mismatch (ABI)%s");
   if (a->B < 0 || a->H < 1 || a->Q < 1 || a->d_latent < 8 || a->d_rope < 0)
     return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: bad B/H/Q/d_latent/d_rope%s");
-  if (a->Q > 64) return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: Q > 64 not supported%s");
+  if (a->mask_mode != TV_MASK_TREE && a->mask_mode != TV_MASK_CAUSAL)
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: bad mask_mode%s");
+  const bool causal = a->mask_mode == TV_MASK_CAUSAL;
+  if (a->Q > 64 && !causal)
+    return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: Q > 64 needs TV_MASK_CAUSAL%s");
+  if ((int64_t)a->B * a->Q * a->H >= (1ll << 31))
+    return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: B*Q*H must be below 2^31%s");
   if (a->d_latent % 8 || a->d_rope % 8)
     return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: d_latent and d_rope must be multiples of 8%s");
   if (!(a->q_dt == TV_F32 || a->q_dt == TV_BF16) || a->q_dt != a->kv_dt)
     return fail(TV_ERR_UNSUPPORTED, "tv_verify_attn: q_dt and kv_dt must both be F32 or BF16%s");
   if (a->max_prefix_len < 0) return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: max_prefix_len < 0%s");
   if (a->B == 0) return TV_OK;
-  if (!a->q_latent || !a->c_kv || !a->prefix_len || !a->anc || !a->out || !a->lse ||
+  if (!a->q_latent || !a->c_kv || !a->prefix_len || (!causal && !a->anc) || !a->out || !a->lse ||
       (a->d_rope > 0 && (!a->q_pe || !a->k_pe)))
     return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: NULL tensor pointer%s");
   const int64_t es = a->kv_dt == TV_BF16 ? 2 : 4;
@@ -145,7 +151,7 @@ int tv_rope_neox(const void* in, tv_dtype in_dt, int64_t in_stride_row,
     return fail(TV_ERR_INVALID_ARG, "tv_rope_neox: bad dtype%s");
   if (!(base > 0.0)) return fail(TV_ERR_INVALID_ARG, "tv_rope_neox: base must be > 0%s");
   if (B == 0) return TV_OK;
-  if (!in || !out || !prefix_len || !depth)
+  if (!in || !out || !prefix_len)
     return fail(TV_ERR_INVALID_ARG, "tv_rope_neox: NULL pointer%s");
   if (in_stride_head < d_rope || out_stride_head < d_rope ||
       in_stride_row < (int64_t)(n_heads - 1) * in_stride_head + d_rope ||
@@ -212,6 +218,76 @@ int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void
     return fail(TV_ERR_WORKSPACE, "tv_verify_attn: workspace smaller than tv_verify_attn_workspace_size()%s");
   cudaError_t e = tv::launch_attn_simt(a, plan, workspace, (cudaStream_t)stream);
   return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_verify_attn");
+}
+
+size_t tv_tree_accept_workspace_size(int B, int Q, int64_t vocab) {
+  if (B < 0 || Q < 1 || Q > 64 || vocab < 1) return 0;
+  return tv::accept_workspace(B, Q, tv::accept_plan(B, Q, vocab, sm_count()));
+}
+
+int tv_tree_accept(const void* logits, tv_dtype logits_dt, int64_t vocab,
+                   int64_t logits_row_stride, const int32_t* parent, const int32_t* tokens,
+                   int B, int Q, int32_t* target, int32_t* accept_len, int32_t* path,
+                   int32_t* new_tokens, int32_t* status, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  g_last_error.clear();
+  if (B < 0 || Q < 1) return fail(TV_ERR_INVALID_ARG, "tv_tree_accept: B < 0 or Q < 1%s");
+  if (Q > 64) return fail(TV_ERR_UNSUPPORTED, "tv_tree_accept: Q > 64 not supported%s");
+  if (!(logits_dt == TV_F32 || logits_dt == TV_BF16))
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_accept: logits must be F32 or BF16%s");
+  if (vocab < 1 || vocab >= 0x7FFFFFFFll || logits_row_stride < vocab)
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_accept: bad vocab or row stride%s");
+  if (B == 0) return TV_OK;
+  if (!logits || !parent || !tokens || !accept_len || !path || !new_tokens)
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_accept: NULL pointer%s");
+  const uintptr_t es = logits_dt == TV_BF16 ? 2 : 4;
+  if ((uintptr_t)logits % es)
+    return fail(TV_ERR_INVALID_ARG, "tv_tree_accept: logits not aligned to its element size%s");
+  const tv::AcceptPlan plan = tv::accept_plan(B, Q, vocab, sm_count());
+  const size_t need = tv::accept_workspace(B, Q, plan);
+  if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < need)
+    return fail(TV_ERR_WORKSPACE, "tv_tree_accept: workspace missing, misaligned or smaller "
+                                  "than tv_tree_accept_workspace_size()%s");
+  cudaError_t e = tv::launch_accept(logits, logits_dt, vocab, logits_row_stride, parent, tokens,
+                                    B, Q, target, accept_len, path, new_tokens, status, plan,
+                                    workspace, (cudaStream_t)stream);
+  return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_tree_accept");
+}
+
+int tv_compact_kv(void* c_kv, void* k_pe, tv_dtype kv_dt, int64_t ckv_row_stride,
+                  int64_t kpe_row_stride, int d_latent, int d_rope,
+                  const tv_cache_layout* cache, const int32_t* prefix_len, const int32_t* path,
+                  const int32_t* accept_len, int B, int Q, int32_t* new_prefix_len,
+                  int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (B < 0 || Q < 1 || d_latent < 0 || d_rope < 0)
+    return fail(TV_ERR_INVALID_ARG, "tv_compact_kv: bad B/Q/d_latent/d_rope%s");
+  if (Q > 64) return fail(TV_ERR_UNSUPPORTED, "tv_compact_kv: Q > 64 not supported%s");
+  if (!(kv_dt == TV_F32 || kv_dt == TV_BF16))
+    return fail(TV_ERR_INVALID_ARG, "tv_compact_kv: bad dtype%s");
+  if (!cache || cache->num_rows <= 0)
+    return fail(TV_ERR_INVALID_ARG, "tv_compact_kv: cache layout with num_rows is required%s");
+  if (B == 0) return TV_OK;
+  if (!c_kv || (d_rope > 0 && !k_pe) || !prefix_len || !path || !accept_len || !new_prefix_len)
+    return fail(TV_ERR_INVALID_ARG, "tv_compact_kv: NULL pointer%s");
+  const int64_t es = kv_dt == TV_BF16 ? 2 : 4;
+  if (ckv_row_stride < d_latent || (d_rope > 0 && kpe_row_stride < d_rope) ||
+      (d_latent * es) % 16 || (d_rope * es) % 16 || (ckv_row_stride * es) % 16 ||
+      (d_rope > 0 && (kpe_row_stride * es) % 16) || !aligned16(c_kv) ||
+      (d_rope > 0 && !aligned16(k_pe)))
+    return fail(TV_ERR_INVALID_ARG,
+                "tv_compact_kv: rows, strides and pointers must be 16-byte multiples%s");
+  tv::CacheGeom g{cache->page_table, cache->page_size, cache->max_pages, cache->kv_stride_b};
+  if (g.page_table && (g.page_size <= 0 || g.max_pages <= 0))
+    return fail(TV_ERR_INVALID_ARG, "tv_compact_kv: paged cache needs page_size and max_pages%s");
+  if (!g.page_table && g.kv_stride_b < Q)
+    return fail(TV_ERR_INVALID_ARG, "tv_compact_kv: kv_stride_b too small%s");
+  cudaError_t e = tv::launch_compact(c_kv, ckv_row_stride * es, d_rope > 0 ? k_pe : c_kv,
+                                     kpe_row_stride * es, (int)(d_latent * es),
+                                     (int)(d_rope * es), g, cache->num_rows, prefix_len, path,
+                                     accept_len, B, Q, new_prefix_len, status,
+                                     (cudaStream_t)stream);
+  return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_compact_kv");
 }
 
 }  // extern "C"

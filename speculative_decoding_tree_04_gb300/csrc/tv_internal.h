@@ -71,6 +71,27 @@ int tc_launch_count(const tv_attn_args* a, const TcPlan& p);  // kernels launch_
 cudaError_t launch_combine(const float* ws_out, const float* ws_lse, int splits,
                            int64_t rows, int DL, float* out, float* lse, cudaStream_t st);
 
+// Greedy tree acceptance: argmax of every node's logits in `chunks` pieces per row, then
+// the walk (k_accept.cu).
+struct AcceptPlan {
+  int chunks;     // pieces per logit row
+  int64_t chunk;  // vocabulary entries per piece (multiple of 2048)
+};
+AcceptPlan accept_plan(int B, int Q, int64_t V, int sm_count);
+size_t accept_workspace(int B, int Q, const AcceptPlan& p);
+cudaError_t launch_accept(const void* logits, tv_dtype dt, int64_t V, int64_t stride,
+                          const int32_t* parent, const int32_t* tokens, int B, int Q,
+                          int32_t* target, int32_t* accept_len, int32_t* path,
+                          int32_t* new_tokens, int32_t* status, const AcceptPlan& p,
+                          void* ws, cudaStream_t st);
+// Post-verify compaction of the accepted nodes' cache rows (k_accept.cu); strides and row
+// sizes in bytes, multiples of 16.
+cudaError_t launch_compact(void* c_kv, int64_t ckv_stride_bytes, void* k_pe,
+                           int64_t kpe_stride_bytes, int ckv_row_bytes, int kpe_row_bytes,
+                           const CacheGeom& g, int64_t num_rows, const int32_t* prefix_len,
+                           const int32_t* path, const int32_t* accept_len, int B, int Q,
+                           int32_t* new_prefix_len, int32_t* status, cudaStream_t st);
+
 // Set the thread-local text returned by tv_last_error() (defined in tv_api.cu).
 void set_last_error(const char* msg);
 

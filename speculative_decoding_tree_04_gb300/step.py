@@ -36,12 +36,16 @@ class VerifyStep:
                  "c_kv", "k_pe")
 
     def __init__(self, inp: dict, device="cuda", path=tv.PATH_AUTO, num_splits=0,
-                 paged_view=tv.PAGED_AUTO):
+                 paged_view=tv.PAGED_AUTO, causal=False):
         self.inp = inp
         self.device = torch.device(device)
         self.path = path
         self.num_splits = num_splits
         self.paged_view = paged_view
+        # causal: prefill of Q tokens after the prefix (no draft tree: no visibility call,
+        # token i at position P + i, the causal mask)
+        self.causal = causal
+        self.mask_mode = tv.MASK_CAUSAL if causal else tv.MASK_TREE
         d = self.device
         B, Q, H, DL = inp["B"], inp["Q"], inp["H"], inp["DL"]
         self.B, self.Q, self.H, self.DL, self.DR = B, Q, H, DL, inp["DR"]
@@ -55,8 +59,8 @@ class VerifyStep:
         self.c_kv = _dev_float(inp, "c_kv", d)
         self.k_pe = _dev_float(inp, "k_pe", d)
         self.q_pe = torch.zeros_like(self.q_pe_raw)
-        self.anc = torch.empty((B, Q), dtype=torch.int64, device=d)
-        self.depth = torch.empty((B, Q), dtype=torch.int32, device=d)
+        self.anc = None if causal else torch.empty((B, Q), dtype=torch.int64, device=d)
+        self.depth = None if causal else torch.empty((B, Q), dtype=torch.int32, device=d)
         self.out = torch.empty((B, Q, H, DL), dtype=torch.float32, device=d)
         self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=d)
         self.status = torch.zeros(1, dtype=torch.int32, device=d)
@@ -69,7 +73,8 @@ class VerifyStep:
         return tv.attn_args(self.q_latent, self.q_pe, self.c_kv, self.k_pe, self.prefix_len,
                             self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
                             self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
-                            self.status, self.path, self.num_splits, self.paged_view)
+                            self.status, self.path, self.num_splits, self.paged_view,
+                            self.mask_mode)
 
     def _alloc_workspace(self):
         need = tv.workspace_size(self.attn_args())
@@ -81,6 +86,8 @@ class VerifyStep:
 
     # -- the four calls of one step ------------------------------------------------
     def visibility(self, stream=None):
+        if self.causal:
+            return  # no tree to resolve
         tv.build_visibility(self.parent, self.anc, self.depth, status=self.status,
                             stream=stream)
 
@@ -97,7 +104,7 @@ class VerifyStep:
                        self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
                        self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
                        self.status, self.path, self.num_splits, workspace=self.workspace,
-                       stream=stream, paged_view=self.paged_view)
+                       stream=stream, paged_view=self.paged_view, mask_mode=self.mask_mode)
 
     def run(self, stream=None):
         self.visibility(stream)
@@ -128,14 +135,15 @@ class VerifyStep:
         return g_pre, g_attn
 
     def launches_per_step(self) -> int:
-        """Kernels one run() enqueues: visibility, 2 RoPE, and the attention call's own."""
-        return 3 + tv.attn_launches(self.attn_args())
+        """Kernels one run() enqueues: visibility (not for causal prefill), 2 RoPE, and the
+        attention call's own."""
+        return (2 if self.causal else 3) + tv.attn_launches(self.attn_args())
 
     # -- results --------------------------------------------------------------------
     def results(self):
         torch.cuda.synchronize(self.device)
-        anc = self.anc.cpu().numpy().view(np.uint64)
-        return dict(anc=anc, depth=self.depth.cpu().numpy(),
+        anc = None if self.anc is None else self.anc.cpu().numpy().view(np.uint64)
+        return dict(anc=anc, depth=None if self.depth is None else self.depth.cpu().numpy(),
                     q_pe_rot=self.q_pe.float().cpu().numpy(),
                     k_pe_cache=self.k_pe.float().cpu().numpy(),
                     out=self.out.cpu().numpy(), lse=self.lse.cpu().numpy(),

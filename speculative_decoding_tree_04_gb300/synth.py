@@ -170,3 +170,58 @@ def sample_sequences(inp: dict, n: int = 4, seed: int = 77) -> np.ndarray:
         list(rng.choice(even, n - k_odd, replace=False))
     return np.sort(np.array(pick, np.int32))
 
+
+
+VOCAB = 163840  # vocabulary of the Kimi-K2-class target model the pages build for
+
+
+def generate_accept(inp: dict, vocab: int = VOCAB, seed: int | None = None,
+                    p_continue: float = 0.75, dtype: str = "fp32", ties: bool = True) -> dict:
+    """Draft tokens and target logits for greedy tree acceptance over ``inp``'s trees.
+
+    tokens [B,Q] int32: a random token per node, distinct among the children of every
+    node unless the vocabulary is smaller than the number of children.  logits [B,Q,vocab] float32 (or bf16-representable values with ``<>_bits``):
+    N(0,1) noise, and along one random root path per sequence the logit of the next path
+    node's token is raised above the row's maximum (the walk continues there with
+    probability p_continue at every step), so that acceptance lengths vary.  With ``ties``
+    some rows get their maximum repeated at a smaller token id (the argmax rule must pick
+    the smaller).  Numbers only: no acceptance logic is computed here."""
+    B, Q = inp["B"], inp["Q"]
+    parent = inp["parent"]
+    seed = (inp.get("seed", 1000) + 7919) if seed is None else seed
+    r_tok, r_log, r_path, r_tie = [np.random.default_rng(s)
+                                   for s in np.random.SeedSequence(seed).spawn(4)]
+    tokens = np.zeros((B, Q), np.int32)
+    for b in range(B):
+        tokens[b, 0] = int(r_tok.integers(0, vocab))
+        for node in range(Q):
+            kids = [c for c in range(1, Q) if parent[b, c] == node]
+            if kids:
+                # distinct sibling tokens when the vocabulary allows it
+                tokens[b, kids] = r_tok.choice(vocab, size=len(kids),
+                                               replace=len(kids) > vocab)
+    logits = r_log.standard_normal((B, Q, vocab), dtype=np.float32)
+    if dtype == "bf16":
+        logits = bf16_to_f32(bf16_bits(logits)).reshape(B, Q, vocab)
+    for b in range(B):
+        cur = 0
+        while True:
+            kids = [c for c in range(1, Q) if parent[b, c] == cur]
+            if not kids or r_path.random() >= p_continue:
+                break
+            c = int(r_path.choice(kids))
+            logits[b, cur, tokens[b, c]] = logits[b, cur].max() + 1.0
+            cur = c
+    if ties:
+        for b in range(B):
+            for i in range(Q):
+                if r_tie.random() < 0.25:
+                    j = int(np.argmax(logits[b, i]))
+                    if j > 0:
+                        logits[b, i, int(r_tie.integers(0, j))] = logits[b, i, j]
+    out = dict(tokens=tokens, logits=logits, vocab=vocab, logits_dtype=dtype)
+    if dtype == "bf16":
+        # planted values are re-rounded (they stay above the row's other values)
+        out["logits_bits"] = bf16_bits(logits)
+        out["logits"] = bf16_to_f32(out["logits_bits"]).reshape(B, Q, vocab)
+    return out

@@ -8,6 +8,8 @@ this module raises.
     build_visibility(parent, anc, depth, dense_mask=None, status=None)
     rope_neox(x, out, prefix_len, depth, base=10000.0, cache=None)
     verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, ...)
+    tree_accept(logits, parent, tokens, accept_len, path, new_tokens, target=None, ...)
+    compact_kv(c_kv, k_pe, cache, prefix_len, path, accept_len, new_prefix_len, ...)
 """
 from __future__ import annotations
 
@@ -26,6 +28,7 @@ TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_ERR_WORKSPACE, TV_ERR_BOUNDS = -4, -5, -6, -7
 TV_F32, TV_BF16 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TCGEN05 = 0, 1, 2
 PAGED_AUTO, PAGED_STEP_MAPS, PAGED_GATHER = 0, 1, 2
+MASK_TREE, MASK_CAUSAL = 0, 1
 
 
 class TVError(RuntimeError):
@@ -59,6 +62,7 @@ class AttnArgs(ctypes.Structure):
         ("path", ctypes.c_int32),
         ("num_splits", ctypes.c_int32),
         ("paged_view", ctypes.c_int32),
+        ("mask_mode", ctypes.c_int32),
     ]
 
 
@@ -90,6 +94,12 @@ def load():
     lib.tv_last_error.restype = ctypes.c_char_p
     lib.tv_version.restype = ctypes.c_int
     lib.tv_testing_set_wait_fault.argtypes = [i32, ctypes.c_uint64, P]
+    lib.tv_tree_accept_workspace_size.argtypes = [i32, i32, i64]
+    lib.tv_tree_accept_workspace_size.restype = ctypes.c_size_t
+    lib.tv_tree_accept.argtypes = [P, i32, i64, i64, P, P, i32, i32, P, P, P, P, P, P,
+                                   ctypes.c_size_t, P]
+    lib.tv_compact_kv.argtypes = [P, P, i32, i64, i64, i32, i32, ctypes.POINTER(CacheLayout),
+                                  P, P, P, i32, i32, P, P, P]
     _lib = lib
     return lib
 
@@ -160,7 +170,8 @@ def make_cache(page_table=None, page_size=64, kv_stride_b=0, num_rows=0) -> Cach
 
 def rope_neox(x, out, prefix_len, depth, base=10000.0, cache: CacheLayout | None = None,
               stream=None):
-    """NeoX RoPE on x [B,Q,H,D] (or [B,Q,D] for one head) into out.
+    """NeoX RoPE on x [B,Q,H,D] (or [B,Q,D] for one head) into out; depth None means row
+    i sits at position prefix_len + i (a chain, as in prefill).
 
     Without ``cache`` out has x's shape (in place allowed).  With ``cache`` out is a cache
     array [rows, D] (row stride out.stride(0)) and row (b, i) goes to the cache slot of
@@ -191,12 +202,12 @@ def rope_neox(x, out, prefix_len, depth, base=10000.0, cache: CacheLayout | None
 
 def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
               page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
-              num_splits=0, paged_view=PAGED_AUTO) -> AttnArgs:
+              num_splits=0, paged_view=PAGED_AUTO, mask_mode=MASK_TREE) -> AttnArgs:
     _need_cuda(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, page_table, status)
     B, Q, H, DL = q_latent.shape
     DR = q_pe.shape[-1]
     for t in (q_latent, q_pe, prefix_len, anc, out, lse):
-        if not t.is_contiguous():
+        if t is not None and not t.is_contiguous():
             raise ValueError("q_latent, q_pe, prefix_len, anc, out, lse must be contiguous")
     if c_kv.stride(-1) != 1 or k_pe.stride(-1) != 1:
         raise ValueError("cache rows must be contiguous")
@@ -212,10 +223,11 @@ def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_
                          min(c_kv.shape[0], k_pe.shape[0]))
     a.prefix_len = prefix_len.data_ptr()
     a.max_prefix_len = int(max_prefix_len)
-    a.anc = anc.data_ptr()
+    a.anc = None if anc is None else anc.data_ptr()
     a.out, a.lse = out.data_ptr(), lse.data_ptr()
     a.status = None if status is None else status.data_ptr()
     a.path, a.num_splits, a.paged_view = int(path), int(num_splits), int(paged_view)
+    a.mask_mode = int(mask_mode)
     return a
 
 
@@ -254,14 +266,15 @@ def noalloc_scratch_bytes() -> int:
 
 def verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
                 page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
-                num_splits=0, workspace=None, stream=None, paged_view=PAGED_AUTO):
+                num_splits=0, workspace=None, stream=None, paged_view=PAGED_AUTO,
+                mask_mode=MASK_TREE):
     """Tree-verify attention; out [B,Q,H,DL] and lse [B,Q,H] (float32) are written.
 
     ``workspace`` (a CUDA uint8 tensor) is allocated through torch and cached per device
     when not given."""
     a = attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale,
                   max_prefix_len, page_table, page_size, kv_stride_b, status, path, num_splits,
-                  paged_view)
+                  paged_view, mask_mode)
     need = workspace_size(a)
     if workspace is None and need > 0:
         key = q_latent.device
@@ -275,3 +288,50 @@ def verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, ma
     rc = load().tv_verify_attn(ctypes.byref(a), wptr, wbytes, _stream(stream))
     _check(rc, "tv_verify_attn")
     return a
+
+
+def accept_workspace_size(B: int, Q: int, vocab: int) -> int:
+    return int(load().tv_tree_accept_workspace_size(B, Q, vocab))
+
+
+def tree_accept(logits, parent, tokens, accept_len, path, new_tokens, target=None,
+                status=None, workspace=None, stream=None):
+    """Greedy acceptance: logits [B,Q,V] (float32 or bf16, rows contiguous) -> accept_len
+    [B], path [B,Q], new_tokens [B,Q] (and target [B,Q] if given), all int32.  The
+    workspace (argmax keys) is allocated through torch and cached when not given."""
+    _need_cuda(logits, parent, tokens, accept_len, path, new_tokens, target, status)
+    B, Q, V = logits.shape
+    if logits.stride(2) != 1 or logits.stride(0) != Q * logits.stride(1):
+        raise ValueError("logits rows must be contiguous and uniformly strided over (B, Q)")
+    for t in (parent, tokens, accept_len, path, new_tokens):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("parent, tokens and the outputs must be contiguous int32")
+    need = accept_workspace_size(B, Q, V)
+    if workspace is None and need > 0:
+        key = ("accept", logits.device)
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=logits.device)
+            _ws_cache[key] = ws
+        workspace = ws
+    wptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().tv_tree_accept(_ptr(logits), _dt(logits), V, logits.stride(1), _ptr(parent),
+                               _ptr(tokens), B, Q, _ptr(target), _ptr(accept_len), _ptr(path),
+                               _ptr(new_tokens), _ptr(status), wptr, wbytes, _stream(stream))
+    _check(rc, "tv_tree_accept")
+
+
+def compact_kv(c_kv, k_pe, cache: CacheLayout, prefix_len, path, accept_len, new_prefix_len,
+               status=None, stream=None):
+    """Post-verify compaction of the cache arrays c_kv [rows, DL] and k_pe [rows, DR] (in
+    place) under ``cache`` (with num_rows set); new_prefix_len [B] int32 is written."""
+    _need_cuda(c_kv, k_pe, prefix_len, path, accept_len, new_prefix_len, status)
+    if c_kv.stride(-1) != 1 or k_pe.stride(-1) != 1:
+        raise ValueError("cache rows must be contiguous")
+    B, Q = path.shape
+    rc = load().tv_compact_kv(_ptr(c_kv), _ptr(k_pe), _dt(c_kv), c_kv.stride(0), k_pe.stride(0),
+                              c_kv.shape[1], k_pe.shape[1], ctypes.byref(cache),
+                              _ptr(prefix_len), _ptr(path), _ptr(accept_len), B, Q,
+                              _ptr(new_prefix_len), _ptr(status), _stream(stream))
+    _check(rc, "tv_compact_kv")

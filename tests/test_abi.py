@@ -110,3 +110,57 @@ def test_rope_argument_errors(tvlib):
     assert call(isr=100) == tv.TV_ERR_INVALID_ARG      # rows overlap
     assert call(in_dt=5) == tv.TV_ERR_INVALID_ARG
     assert call(B=0) == tv.TV_OK                        # nothing to do, nothing launched
+
+
+def test_tree_accept_argument_errors(tvlib):
+    lib = tv.load()
+    f = lib.tv_tree_accept
+    ws = lib.tv_tree_accept_workspace_size(4, 9, 163840)
+    assert ws > 0 and ws % 256 == 0
+    assert lib.tv_tree_accept_workspace_size(4, 65, 100) == 0
+
+    def call(B=4, Q=9, V=163840, stride=163840, dt=tv.TV_F32, logits=FAKE, wsp=FAKE, wsb=ws):
+        return f(logits, dt, V, stride, FAKE, FAKE, B, Q, None, FAKE, FAKE, FAKE, None, wsp, wsb,
+                 None)
+
+    assert call(Q=65) == tv.TV_ERR_UNSUPPORTED
+    assert call(Q=0) == tv.TV_ERR_INVALID_ARG
+    assert call(V=0) == tv.TV_ERR_INVALID_ARG
+    assert call(stride=100) == tv.TV_ERR_INVALID_ARG          # stride < vocab
+    assert call(logits=FAKE + 2) == tv.TV_ERR_INVALID_ARG      # not float-aligned
+    assert call(dt=7) == tv.TV_ERR_INVALID_ARG
+    assert call(wsp=None) == tv.TV_ERR_WORKSPACE
+    assert call(wsb=ws - 8) == tv.TV_ERR_WORKSPACE
+    assert call(wsp=FAKE + 64) == tv.TV_ERR_WORKSPACE
+    assert call(B=0) == tv.TV_OK
+
+
+def test_compact_kv_argument_errors(tvlib):
+    lib = tv.load()
+    f = lib.tv_compact_kv
+    good = tv.CacheLayout(FAKE, 64, 10, 0, 6400)
+
+    def call(dt=tv.TV_BF16, DL=512, DR=64, ck=FAKE, cache=good, Q=9):
+        return f(ck, FAKE, dt, DL, DR, DL, DR, ctypes.byref(cache) if cache else None, FAKE,
+                 FAKE, FAKE, 2, Q, FAKE, None, None)
+
+    assert call(Q=65) == tv.TV_ERR_UNSUPPORTED
+    assert call(cache=None) == tv.TV_ERR_INVALID_ARG
+    assert call(cache=tv.CacheLayout(FAKE, 64, 10, 0, 0)) == tv.TV_ERR_INVALID_ARG  # rows
+    assert call(DR=4) == tv.TV_ERR_INVALID_ARG                # 8-byte rows
+    assert call(ck=FAKE + 8) == tv.TV_ERR_INVALID_ARG
+    assert call(dt=9) == tv.TV_ERR_INVALID_ARG
+    assert call(cache=tv.CacheLayout(FAKE, 0, 10, 0, 6400)) == tv.TV_ERR_INVALID_ARG
+
+
+def test_causal_mask_allows_long_q_without_anc(tvlib):
+    # prefill: Q beyond 64 and no ancestor bitsets with the causal mask
+    assert path_of(fake_args(Q=4096, anc=None, mask_mode=tv.MASK_CAUSAL,
+                             cache=tv.CacheLayout(None, 64, 0, 8192))) == tv.PATH_SIMT
+    assert path_of(fake_args(Q=4096, mask_mode=tv.MASK_TREE,
+                             cache=tv.CacheLayout(None, 64, 0, 8192))) == tv.TV_ERR_UNSUPPORTED
+    assert path_of(fake_args(anc=None)) == tv.TV_ERR_INVALID_ARG       # tree mode needs anc
+    assert path_of(fake_args(mask_mode=2)) == tv.TV_ERR_INVALID_ARG
+    # B*Q*H must stay below 2^31
+    assert path_of(fake_args(B=1 << 12, Q=1 << 14, H=64, mask_mode=tv.MASK_CAUSAL, anc=None,
+                             cache=tv.CacheLayout(None, 64, 0, 1 << 15))) == tv.TV_ERR_UNSUPPORTED

@@ -408,7 +408,7 @@ def main():
                     help="override the workload's batch size (smaller profiler captures)")
     ap.add_argument("--also", default=None,
                     help="comma-separated further workloads timed the same way and reported "
-                         "under 'configs' (default: cfg4_bf16 beside cfg5_bf16)")
+                         "under 'configs' (default: cfg4_bf16 and prefill_bf16 beside cfg5_bf16)")
     ap.add_argument("--quick", action="store_true",
                     help="device-timed steps only (no end-to-end pass, no CPU baseline); "
                          "used for profiler runs")
@@ -521,7 +521,7 @@ def main():
     # ---- further workloads, the same protocol (reported under "configs") ------------
     also = args.also
     if also is None:
-        also = "cfg4_bf16" if args.workload == "cfg5_bf16" and args.batch == 0 else ""
+        also = "cfg4_bf16,prefill_bf16" if args.workload == "cfg5_bf16" and args.batch == 0 else ""
     peaks = load_peaks()
     configs = {}
     for name in [w for w in also.split(",") if w]:

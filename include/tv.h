@@ -191,7 +191,8 @@ typedef struct {
   float* lse;               /* device [B, Q, H] float32 out (natural log) */
   int32_t* status;          /* device int32, nullable (see conventions) */
   int32_t path;             /* tv_path; TV_PATH_AUTO normally */
-  int32_t num_splits;       /* 0 = automatic; else force this many KV splits */
+  int32_t num_splits;       /* 0 = automatic; else cut every KV sweep into this many
+                               pieces (tensor cores: each 128-row tile's sweep) */
   int32_t paged_view;       /* tv_paged_view; TV_PAGED_AUTO normally */
   int32_t mask_mode;        /* tv_mask_mode; TV_MASK_TREE for tree verification */
 } tv_attn_args;
@@ -208,7 +209,8 @@ int tv_verify_attn_path(const tv_attn_args* a);
 
 /* How many kernels one tv_verify_attn call with these arguments enqueues (for launch
  * accounting; the CUDA-core path: attention + split combine; the tensor-core path: work
- * preparation + key gather for a large paged cache + attention + split combine), or a
+ * preparation + key gather for a large paged cache + attention + the merge of split
+ * tiles unless num_splits == 1), or a
  * negative tv_status if the arguments are invalid. */
 int tv_verify_attn_launches(const tv_attn_args* a);
 

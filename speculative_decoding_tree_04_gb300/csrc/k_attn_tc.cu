@@ -94,6 +94,10 @@ constexpr int kSideA = kStgOff + kNStg * (int)kMsgBytes;
 constexpr int kInboxOff = kNLO * kHalfO;
 constexpr int kSideB = kInboxOff + kNInbox * kMsgStride;
 constexpr int kSideMax = kSideA > kSideB ? kSideA : kSideB;
+// O side: the epilogue's staging chunks (4 warps x 32 rows x 32 fp32) after the inbox
+constexpr int kEpiOff = kSideB;
+static_assert(kEpiOff + 4 * 32 * 32 * 4 <= kSideMax, "epilogue staging must fit");
+
 constexpr uint32_t kTmQ = 0, kTmS0 = 256, kTmS1 = 384;       // S-side TMEM columns
 constexpr uint32_t kFlagRescale = 2;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // deadline of every wait (wall clock)
@@ -116,13 +120,15 @@ struct TcParams {
   const uint64_t* anc;
   float* out;
   float* lse;
-  float* ws_out;
-  float* ws_lse;
+  float* ws_out;       // partial outputs of split tiles: [slot][128 rows][512]
+  float* ws_lse;       // their log-sum-exps: [slot][128 rows]
+
   int32_t* status;
   int64_t rows_total;  // B*Q*H
   int32_t B, H, Q, max_prefix;
-  int32_t tiles_per_seq, splits, chunk, n_items;
-  const int4* info;  // per work item: sequence, split, tile, prefix length (longest first)
+  int32_t tiles_per_seq;
+  const int4* items;     // per work item two records: {b, t, s0, s1}, {P, pieces, slot, base}
+  const int32_t* cl_start;  // cluster c takes items cl_start[c] .. cl_start[c+1]-1
   float scale_log2;
   uint64_t timeout_ns;        // deadline of every wait
   int32_t causal;             // TV_MASK_CAUSAL: row (node i, head) sees keys 0 .. P + i
@@ -148,53 +154,63 @@ struct Shared {
 // the dynamic window starts 1024-byte aligned, as the swizzled tiles need, without padding).
 constexpr int kSmemBytes = kSideMax + (int)((sizeof(Shared) + 15) / 16 * 16);
 
+// A work item is a piece of a 128-row tile's key sweep: 128-key steps s0 .. s1-1.  A tile
+// cut into several pieces (np > 1) has them written as partial results (the output
+// normalised by the piece's own softmax sum, and its log-sum-exp) into consecutive slots
+// from `base`; merge_kernel combines them after the attention kernel.
 struct Item {
-  int b, t, s, P, nb;
+  int b, t, P, nb;
   int ns;   // 128-key steps: ceil(nb / 2)
   int rot;  // first step of this tile's sweep (see decode)
-  int64_t k0;
+  int np, slot, base;
+  int64_t k0, k1;
   bool bad;
 };
 
-// Work item k of the schedule, from its record (one 16-byte load).
-__device__ __forceinline__ int4 item_info(const TcParams& p, int item) { return __ldg(p.info + item); }
+// Work item k of the schedule, from its two 16-byte records.
+__device__ __forceinline__ int4 item_rec(const TcParams& p, int item, int h) {
+  return __ldg(p.items + 2 * item + h);
+}
 
-__device__ __noinline__ Item decode_info(const TcParams& p, int4 v) {
+__device__ __noinline__ Item decode_info(const TcParams& p, int4 a, int4 v) {
   Item it;
-  it.b = v.x;
-  it.s = v.y;
-  it.t = v.z;
-  it.P = v.w;
+  it.b = a.x;
+  it.t = a.y;
+  it.P = v.x;
+  it.np = v.y;
+  it.slot = v.z;
+  it.base = v.w;
   const int64_t kv_len = (int64_t)it.P + p.Q;
   it.bad = it.P < 0 || it.P > p.max_prefix || kv_len > p.seq_cap;
-  it.k0 = (int64_t)it.s * p.chunk;
   int64_t kend = kv_len;
   if (p.causal) {
     // no row of the tile sees past its last row's node
     const int64_t hi = ((int64_t)(it.t + 1) * kRows - 1) / p.H;
     kend = (int64_t)it.P + (hi < p.Q - 1 ? hi : p.Q - 1) + 1;
   }
-  int64_t k1 = it.k0 + p.chunk < kend ? it.k0 + p.chunk : kend;
-  if (it.bad) k1 = it.k0;
+  it.k0 = (int64_t)a.z * kStep;
+  int64_t k1 = (int64_t)a.w * kStep < kend ? (int64_t)a.w * kStep : kend;
+  if (it.bad || k1 < it.k0) k1 = it.k0;
+  it.k1 = k1;
   it.nb = k1 > it.k0 ? (int)((k1 - it.k0 + kBN - 1) / kBN) : 0;
   it.ns = (it.nb + 1) >> 1;
-  // The row tiles of one sequence run at the same time on neighbouring clusters; each
-  // starts its sweep over the key steps at a different step so that they do not all
+  // The row tiles of one sequence run at the same time on neighbouring clusters; a whole
+  // tile starts its sweep over the key steps at a step of its own so that they do not all
   // request the same cache lines at once (the softmax is independent of block order).
-  it.rot = it.ns > 0 ? (int)(((int64_t)it.t * it.ns) / p.tiles_per_seq) : 0;
+  it.rot = (it.ns > 0 && a.z == 0 && k1 == kend) ? (int)(((int64_t)it.t * it.ns) / p.tiles_per_seq)
+                                                  : 0;
   return it;
 }
 
 __device__ __forceinline__ Item decode(const TcParams& p, int item) {
-  return decode_info(p, item_info(p, item));
+  return decode_info(p, item_rec(p, item, 0), item_rec(p, item, 1));
 }
 
-// Item taken by cluster `cid` in round r, or -1 when it has none left.  Items are sorted
-// longest first and dealt out in snake order (rounds alternate direction), which evens
-// out the clusters' total work.
-__device__ __forceinline__ int item_at(const TcParams& p, int r, int cid, int ncl) {
-  const int k = r * ncl + ((r & 1) ? ncl - 1 - cid : cid);
-  return k < p.n_items ? k : -1;
+// Item taken by cluster `cid` in round r, or -1 when it has none left (each cluster works
+// through its own list of the schedule, see schedule_kernel).
+__device__ __forceinline__ int item_at(const TcParams& p, int r, int cid, int) {
+  const int k = __ldg(p.cl_start + cid) + r;
+  return k < __ldg(p.cl_start + cid + 1) ? k : -1;
 }
 
 // 128-key step visited at position j of the tile's sweep; it holds the 64-key blocks
@@ -537,26 +553,26 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
     // The next item's record is requested a whole tile ahead (its queries reach TMEM
     // without these warps).
     int item_next = item_at(p, 0, cid, ncl);
-    int4 info_next = item_next >= 0 ? item_info(p, item_next) : make_int4(0, 0, 0, 0);
+    int4 info_next = item_next >= 0 ? item_rec(p, item_next, 0) : make_int4(0, 0, 0, 0);
+    int4 info_next2 = item_next >= 0 ? item_rec(p, item_next, 1) : make_int4(0, 0, 0, 0);
     for (int rr = 0; item_next >= 0 && live; ++rr) {
-      const Item it = decode_info(p, info_next);
+      const Item it = decode_info(p, info_next, info_next2);
       item_next = item_at(p, rr + 1, cid, ncl);
-      if (item_next >= 0) info_next = item_info(p, item_next);
+      if (item_next >= 0) {
+        info_next = item_rec(p, item_next, 0);
+        info_next2 = item_rec(p, item_next, 1);
+      }
       const int trow = it.t * kRows + r;
       const bool vrow = trow < p.Q * p.H;
       const int64_t grow = (int64_t)it.b * p.Q * p.H + trow;
-      float* lse_dst = p.splits == 1 ? p.lse + grow : p.ws_lse + (int64_t)it.s * p.rows_total + grow;
-      if (it.bad && r == 0 && it.t == 0 && it.s == 0) report(p.status, TV_ERR_BOUNDS);
-      if (it.nb == 0) {
-        if (vrow) *lse_dst = -INFINITY;
-        continue;
-      }
+      // a whole tile's lse goes to the output; a piece's to its slot
+      float* lse_dst = it.np == 1 ? p.lse + grow : p.ws_lse + (int64_t)it.slot * kRows + r;
+      if (it.nb == 0) continue;  // nothing to compute: the O side writes the empty result
       const int node = trow / p.H;
       const uint64_t anc = (vrow && !p.causal) ? p.anc[(int64_t)it.b * p.Q + node] : 0ull;
       // every key below pv is visible: the prefix, or for a causal row all keys up to its own
       const int64_t pv = p.causal ? (int64_t)it.P + node + 1 : (int64_t)it.P;
-      const int64_t kv_end = (int64_t)it.P + p.Q;
-      const int64_t k1 = it.k0 + p.chunk < kv_end ? it.k0 + p.chunk : kv_end;
+      const int64_t k1 = it.k1;
 
 
       float m = -INFINITY, l = 0.f;
@@ -566,7 +582,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         if (j == (it.ns > 3 ? it.ns - 3 : 0) && item_next >= 0) {
           // warm L2 with the next tile's queries a few steps before they are needed (the
           // key stream would evict lines fetched much earlier)
-          const int nrow = info_next.z * kRows + r;
+          const int nrow = info_next.y * kRows + r;
           if (nrow < p.Q * p.H) {
             const int64_t ng = (int64_t)info_next.x * p.Q * p.H + nrow;
             const char* qlp = reinterpret_cast<const char*>(p.q_latent + ng * kDL);
@@ -659,6 +675,8 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           reinterpret_cast<float*>(stg1 + kMsgL)[r] = l;
           if (r == 0) *reinterpret_cast<uint4*>(stg1 + kMsgFlags) = make_uint4(0u, 0u, 0u, 0u);
         }
+        if (j == it.ns - 1 && vrow)  // the tile's (or piece's) log-sum-exp
+          *lse_dst = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         fence_proxy_async_smem();  // the bulk copies read the staging through the async proxy
         named_sync(3, 128);
         if (r == 0) {
@@ -675,8 +693,6 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
         mc += two ? 2 : 1;
       }
       if (!live) break;
-      if (vrow && !sh.abort)
-        *lse_dst = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
     if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
@@ -812,15 +828,19 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
       const int trow = it.t * kRows + r;
       const bool vrow = trow < p.Q * p.H;
       const int64_t grow = (int64_t)it.b * p.Q * p.H + trow;
-      float* dst = p.splits == 1 ? p.out + grow * kDL
-                                 : p.ws_out + ((int64_t)it.s * p.rows_total + grow) * kDL;
+      // a whole tile goes to the output, a piece of a split tile to its slot
+      float* dst = it.np == 1 ? p.out + grow * kDL
+                              : p.ws_out + ((int64_t)it.slot * kRows + r) * kDL;
+      if (it.bad && r == 0) report(p.status, TV_ERR_BOUNDS);
       if (it.nb == 0) {
-        if (vrow)
+        // no visible key in this item (an empty piece or an out-of-range prefix)
+        if (vrow) {
           for (int c = 0; c < kDL / 4; ++c)
             reinterpret_cast<float4*>(dst)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        continue;
+          *(it.np == 1 ? p.lse + grow : p.ws_lse + (int64_t)it.slot * kRows + r) = -INFINITY;
+        }
       }
-      for (;;) {
+      for (; it.nb > 0;) {
         // the four warps work on disjoint TMEM lanes; each warp agrees on the outcome
         if (!__all_sync(0xffffffffu, wait_bar(sh, &sh.job_full, jc & 1, p.status))) return;
         ++jc;
@@ -847,18 +867,34 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
         } else if (type == 2) {
           const float lr = reinterpret_cast<const float*>(inbox + pb * kMsgStride + kMsgL)[r];
           const float inv = lr > 0.f ? 1.f / lr : 0.f;
+          // Each thread holds its own row (TMEM lane), so storing straight from registers
+          // would make every warp store touch 32 rows.  Each 32-row x 32-column chunk is
+          // staged in shared memory instead (16-byte pieces XOR-swizzled by row, so that both
+          // the writes and the reads below are free of bank conflicts) and written back with
+          // lanes along the columns: every store instruction fills four whole 128-byte lines.
+          float* stg = reinterpret_cast<float*>(smem + kEpiOff) + wq * 1024;
+          const int wrow0 = it.t * kRows + wq * 32;  // tile row of this warp's lane 0
+          const int rows_ok = p.Q * p.H - wrow0;     // valid rows of the warp's 32
+          float* dst0 = dst - (int64_t)lane * kDL;   // row of lane 0
+          const int rr4 = lane >> 3, jj = lane & 7;
 #pragma unroll 1
           for (int c = 0; c < 16; ++c) {
             uint32_t v[32];
             __syncwarp();
             tmem_ld32(tmem + lane_base + 32 * c, v);
             tmem_wait_ld();
-            if (vrow) {
-              float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                d4[e] = make_float4(__uint_as_float(v[4 * e]) * inv, __uint_as_float(v[4 * e + 1]) * inv,
-                                    __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
+            for (int e = 0; e < 8; ++e)
+              *reinterpret_cast<float4*>(stg + lane * 32 + ((e ^ (lane & 7)) << 2)) =
+                  make_float4(__uint_as_float(v[4 * e]) * inv, __uint_as_float(v[4 * e + 1]) * inv,
+                              __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int row = 4 * i + rr4;
+              const float4 x = *reinterpret_cast<const float4*>(stg + row * 32 + ((jj ^ (row & 7)) << 2));
+              if (row < rows_ok)
+                *reinterpret_cast<float4*>(dst0 + (int64_t)row * kDL + 32 * c + 4 * jj) = x;
             }
           }
           tc_fence_before();
@@ -986,11 +1022,280 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
   }
 }
 
+// ---- work schedule ---------------------------------------------------------------------
+// The work is B * tiles_per_seq row tiles of 128 rows, tile (b, t) sweeping ns(b, t)
+// 128-key steps.  Tiles are listed longest first: with the tree mask all tiles of a
+// sequence are equally long and sequences are ranked by their key count (then tiles
+// follow sequence by sequence, so that the tiles of one sequence run side by side and share
+// its keys through L2); with the causal mask a tile's keys end at its last row, so tiles go
+// from the last tile index down, sequences ranked within each.
+//   - Automatic: the first R = floor(tiles / clusters) rounds deal whole tiles, one per
+//     cluster per round, in snake order (rounds alternate direction).  The remaining
+//     tiles' steps are then cut into equal quotas, one per cluster (stream-K): a tile may
+//     end up in several pieces on consecutive clusters.  A quota is at least kMinPiece
+//     steps and cuts no tile into more than kMaxPieces pieces.
+//   - Forced (num_splits = S): every tile in S pieces of equal step counts, the items in
+//     tile order dealt to the clusters in equal contiguous runs.
+// Each cluster's items are stored consecutively (cl_start[c] .. cl_start[c+1]-1;
+// cl_start[ncl+1] holds the number of partial-result slots used).  The pieces of a split
+// tile get consecutive slots; slot_info[slot] = {b, t, pieces, first slot}.
+constexpr int kMinPiece = 4;
+constexpr int kMaxPieces = 8;
+constexpr int kMaxRanked = 1024;
+constexpr int kMaxSchedClusters = 1024;
+constexpr int kMaxForcedSplits = 32;
+
+struct SchedArgs {
+  const int32_t* prefix_len;
+  int B, Q, H, T, causal, max_prefix;
+  int64_t seq_cap;
+  int ncl, splits, max_slots;
+  int4* items;
+  int32_t* cl_start;
+  int4* slot_info;
+  int32_t* status;
+};
+
+// 128-key steps tile t of a sequence with prefix P sweeps (0 for an out-of-range prefix)
+__device__ __forceinline__ int tile_steps(const SchedArgs& a, int P, int t) {
+  const int64_t kv = (int64_t)P + a.Q;
+  if (P < 0 || P > a.max_prefix || kv > a.seq_cap) return 0;
+  int64_t kend = kv;
+  if (a.causal) {
+    const int64_t hi = ((int64_t)(t + 1) * kRows - 1) / a.H;
+    kend = (int64_t)P + (hi < a.Q - 1 ? hi : a.Q - 1) + 1;
+  }
+  return (int)((kend + kStep - 1) / kStep);
+}
+
+// Exclusive prefix sums of val(i), i < n, over the block (1024 threads, warp shuffles):
+// written to out (nullable); returns the total to every thread.
+template <class F>
+__device__ int block_scan(int n, F val, int32_t* out, int* sh) {
+  const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += val(i);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    sh[32 + lane] = w;  // inclusive totals of warps 0 .. lane
+  }
+  __syncthreads();
+  const int total = sh[32 + (int)(blockDim.x >> 5) - 1];
+  int run = inc - sum + (warp > 0 ? sh[32 + warp - 1] : 0);
+  if (out)
+    for (int i = lo; i < hi; ++i) {
+      out[i] = run;
+      run += val(i);
+    }
+  __syncthreads();
+  return total;
+}
+
+__device__ void schedule(const SchedArgs& a) {
+  // All scratch stays in shared memory: fewer tiles remain for the quotas than there are
+  // clusters (<= kMaxSchedClusters).
+  __shared__ int order[kMaxRanked];
+  __shared__ int sp[kMaxRanked];  // prefix length of every sequence (when B <= kMaxRanked)
+  __shared__ int scan[64];
+  __shared__ int cnt[kMaxSchedClusters], first[kMaxSchedClusters];
+  __shared__ int su[kMaxSchedClusters], sbase[kMaxSchedClusters], scl[kMaxSchedClusters + 1];
+  __shared__ int s_max;
+  const int B = a.B, T = a.T, ncl = a.ncl;
+  const int n_tiles = B * T;
+  const bool ranked = B <= kMaxRanked;
+  for (int i = threadIdx.x; ranked && i < B; i += blockDim.x) sp[i] = a.prefix_len[i];
+  __syncthreads();
+  auto P_of = [&](int b) { return ranked ? sp[b] : a.prefix_len[b]; };
+  // sequences longest first (ties by index); beyond kMaxRanked the identity
+  for (int i = threadIdx.x; ranked && i < B; i += blockDim.x) {
+    const int ci = tile_steps(a, sp[i], T - 1);
+    int rank = 0;
+    for (int j = 0; j < B; ++j) {
+      const int cj = tile_steps(a, sp[j], T - 1);
+      rank += (cj > ci) || (cj == ci && j < i);
+    }
+    order[rank] = i;
+  }
+  __syncthreads();
+  auto seq_of = [&](int q) { return ranked ? order[q] : q; };
+  // position in the longest-first tile list -> (sequence, tile)
+  auto tile_at = [&](int pos, int& b, int& t) {
+    if (a.causal) {
+      t = T - 1 - pos / B;
+      b = seq_of(pos % B);
+    } else {
+      t = pos % T;
+      b = seq_of(pos / T);
+    }
+  };
+  auto put = [&](int k, int b, int t, int s0, int s1, int np, int slot, int base) {
+    a.items[2 * k] = make_int4(b, t, s0, s1);
+    a.items[2 * k + 1] = make_int4(P_of(b), np, slot, base);
+    if (slot >= 0) a.slot_info[slot] = make_int4(b, t, np, base);
+  };
+
+  if (a.splits > 0) {
+    const int S = a.splits;
+    const int n_items = n_tiles * S;
+    for (int k = threadIdx.x; k < n_items; k += blockDim.x) {
+      const int pos = k / S, j = k - pos * S;
+      int b, t;
+      tile_at(pos, b, t);
+      const int ns = tile_steps(a, P_of(b), t);
+      put(k, b, t, (int)((int64_t)j * ns / S), (int)((int64_t)(j + 1) * ns / S), S,
+          S > 1 ? k : -1, S > 1 ? pos * S : -1);
+    }
+    for (int c = threadIdx.x; c <= ncl; c += blockDim.x)
+      a.cl_start[c] = (int)(((int64_t)c * n_items + ncl - 1) / ncl);
+    if (threadIdx.x == 0) a.cl_start[ncl + 1] = S > 1 ? n_items : 0;
+    return;
+  }
+
+  const int R = n_tiles / ncl;  // rounds of whole tiles
+  const int nd = R * ncl;
+  const int nr = n_tiles - nd;  // tiles left for the quotas
+  if (threadIdx.x == 0) s_max = 0;
+  for (int c = threadIdx.x; c < ncl; c += blockDim.x) {
+    cnt[c] = 0;
+    first[c] = 0x7fffffff;
+  }
+  __syncthreads();
+  auto rem_steps = [&](int i) {
+    int b, t;
+    tile_at(nd + i, b, t);
+    return tile_steps(a, P_of(b), t);
+  };
+  const int W = block_scan(nr, rem_steps, su, scan);
+  for (int i = threadIdx.x; i < nr; i += blockDim.x) atomicMax(&s_max, rem_steps(i));
+  __syncthreads();
+  int q = max((W + ncl - 1) / ncl, kMinPiece);
+  q = max(q, (s_max + kMaxPieces - 1) / kMaxPieces);
+  // clusters a remaining tile touches: [c0, c1]
+  auto span = [&](int i, int& c0, int& c1) {
+    const int u = su[i], ns = rem_steps(i);
+    c0 = min(u / q, ncl - 1);
+    c1 = ns > 0 ? min((u + ns - 1) / q, ncl - 1) : c0;
+  };
+  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+    int c0, c1;
+    span(i, c0, c1);
+    for (int c = c0; c <= c1; ++c) {
+      atomicAdd(&cnt[c], 1);
+      atomicMin(&first[c], i);
+    }
+  }
+  __syncthreads();
+  auto split_slots = [&](int i) {
+    int c0, c1;
+    span(i, c0, c1);
+    return c1 > c0 ? c1 - c0 + 1 : 0;
+  };
+  const int n_slots = block_scan(nr, split_slots, sbase, scan);
+  if (n_slots > a.max_slots) {  // cannot happen (at most two split pieces per cluster)
+    if (threadIdx.x == 0) {
+      report(a.status, TV_ERR_UNSUPPORTED);
+      a.cl_start[ncl + 1] = 0;
+    }
+    for (int c = threadIdx.x; c <= ncl; c += blockDim.x) a.cl_start[c] = 0;
+    return;
+  }
+  const int n_items = block_scan(ncl, [&](int c) { return R + cnt[c]; }, scl, scan);
+  for (int c = threadIdx.x; c < ncl; c += blockDim.x) a.cl_start[c] = scl[c];
+  if (threadIdx.x == 0) {
+    a.cl_start[ncl] = n_items;
+    a.cl_start[ncl + 1] = n_slots;
+  }
+  // whole tiles of the first R rounds
+  for (int pos = threadIdx.x; pos < nd; pos += blockDim.x) {
+    const int r = pos / ncl, i = pos - r * ncl;
+    const int c = (r & 1) ? ncl - 1 - i : i;
+    int b, t;
+    tile_at(pos, b, t);
+    put(scl[c] + r, b, t, 0, tile_steps(a, P_of(b), t), 1, -1, -1);
+  }
+  // pieces of the remaining tiles
+  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+    int c0, c1, b, t;
+    span(i, c0, c1);
+    tile_at(nd + i, b, t);
+    const int u = su[i], ns = rem_steps(i), np = c1 - c0 + 1;
+    for (int c = c0; c <= c1; ++c) {
+      const int s0 = ns > 0 ? max(u, c * q) - u : 0;
+      const int s1 = ns > 0 ? min(u + ns, (c + 1) * q) - u : 0;
+      put(scl[c] + R + (i - first[c]), b, t, s0, s1, np, np > 1 ? sbase[i] + (c - c0) : -1,
+          np > 1 ? sbase[i] : -1);
+    }
+  }
+}
+
+// Merge of split tiles, after the attention kernel: one warp per row of a tile whose
+// first slot is blockIdx.x (8 rows per block).  Lane k < pieces takes piece k's
+// log-sum-exp; then, in slot order,
+//   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) out_k
+// with four 16-byte columns per lane in flight.
+__global__ void __launch_bounds__(256)
+merge_kernel(const int4* __restrict__ slot_info, const int32_t* __restrict__ n_slots,
+             const float* __restrict__ ws_out, const float* __restrict__ ws_lse, int rows_seq,
+             float* __restrict__ out, float* __restrict__ lse) {
+  const int s = blockIdx.x;
+  if (s >= __ldg(n_slots)) return;
+  const int4 si = __ldg(slot_info + s);  // {b, t, pieces, first slot}
+  if (si.w != s) return;                 // not the first slot of its tile
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.y * 8 + warp;
+  const int trow = si.y * kRows + row;
+  if (trow >= rows_seq) return;
+  const int64_t grow = (int64_t)si.x * rows_seq + trow;
+  const int np = si.z;
+  const float ls = lane < np ? ws_lse[(int64_t)(s + lane) * kRows + row] : -INFINITY;
+  float mx = ls;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float e = (lane < np && mx != -INFINITY && ls != -INFINITY) ? expf(ls - mx) : 0.f;
+  float wsum = 0.f;
+  for (int k = 0; k < np; ++k) wsum += __shfl_sync(0xffffffffu, e, k);
+  const float w = wsum > 0.f ? e / wsum : 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < np; ++k) {
+    const float wk = __shfl_sync(0xffffffffu, w, k);
+    if (wk == 0.f) continue;  // the same for the whole warp
+    const float4* src = reinterpret_cast<const float4*>(ws_out + ((int64_t)(s + k) * kRows + row) * kDL);
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldcs(src + lane + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[i].x = fmaf(wk, v[i].x, acc[i].x);
+      acc[i].y = fmaf(wk, v[i].y, acc[i].y);
+      acc[i].z = fmaf(wk, v[i].z, acc[i].z);
+      acc[i].w = fmaf(wk, v[i].w, acc[i].w);
+    }
+  }
+  float4* d4 = reinterpret_cast<float4*>(out + grow * kDL);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[lane + 32 * i] = acc[i];
+  if (lane == 0) lse[grow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
 // Work preparation, one launch before the attention kernel.
-//  - Block 0 orders the (sequence, split) pairs by their number of key blocks, longest
-//    first (ties by index), and writes one record per work item (sequence, split, tile,
-//    prefix length) for the snake schedule.  Beyond kMaxRanked pairs the order stays the
-//    identity.
+//  - Block 0 writes the work schedule (schedule(), above).
 //  - Paged cache: the other blocks write, for every 128-key step of every sequence, the
 //    step's two tensor maps (latent and rope).  Each is a copy of a host-encoded template
 //    with a new base (the step's lower page), page-dimension stride (distance to its other
@@ -998,16 +1303,17 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
 //    1 (the missing half reads as zeros).  A page index outside the cache rows is reported
 //    as TV_ERR_BOUNDS and replaced by page 0 (that sequence's result is then undefined, as
 //    for any out-of-range input).
-constexpr int kMaxRanked = 1024;
 __global__ void __launch_bounds__(1024)
-prep_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, int chunk,
-            int max_prefix, int64_t seq_cap, int tiles, int n_items, int4* __restrict__ info,
-            const __grid_constant__ CUtensorMap tmpl_lat, const __grid_constant__ CUtensorMap tmpl_rope,
-            const unsigned char* ckv, int64_t ckv_page_bytes, const unsigned char* kpe,
-            int64_t kpe_page_bytes, const int32_t* __restrict__ page_table, int max_pages,
-            int64_t num_pages, int steps_per_seq, CUtensorMap* __restrict__ maps,
-            uint8_t* __restrict__ swap, int causal, int32_t* status) {
+prep_kernel(const SchedArgs sa, const __grid_constant__ CUtensorMap tmpl_lat,
+            const __grid_constant__ CUtensorMap tmpl_rope, const unsigned char* ckv,
+            int64_t ckv_page_bytes, const unsigned char* kpe, int64_t kpe_page_bytes,
+            const int32_t* __restrict__ page_table, int max_pages, int64_t num_pages,
+            int steps_per_seq, CUtensorMap* __restrict__ maps, uint8_t* __restrict__ swap) {
   griddep_launch_dependents();  // the attention kernel may start its set-up now
+  const int32_t* prefix_len = sa.prefix_len;
+  const int B = sa.B, Q = sa.Q, max_prefix = sa.max_prefix;
+  const int64_t seq_cap = sa.seq_cap;
+  int32_t* status = sa.status;
   if (blockIdx.x > 0) {
     const int64_t idx = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
     if (idx >= (int64_t)B * steps_per_seq) return;
@@ -1047,43 +1353,7 @@ prep_kernel(const int32_t* __restrict__ prefix_len, int B, int Q, int splits, in
     tmap_release();
     return;
   }
-  __shared__ int cost[kMaxRanked];
-  __shared__ int order[kMaxRanked];
-  const int n = B * splits;
-  const bool ranked = n <= kMaxRanked;
-  for (int i = threadIdx.x; ranked && i < n; i += blockDim.x) {
-    const int b = i / splits, sp = i - b * splits;
-    const int P = prefix_len[b];
-    const int64_t kv = (int64_t)P + Q;
-    const int64_t k0 = (int64_t)sp * chunk;
-    const int64_t k1 = k0 + chunk < kv ? k0 + chunk : kv;
-    const bool bad = P < 0 || P > max_prefix || kv > seq_cap;
-    cost[i] = (bad || k1 <= k0) ? 0 : (int)((k1 - k0 + kBN - 1) / kBN);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; ranked && i < n; i += blockDim.x) {
-    const int ci = cost[i];
-    int rank = 0;
-    for (int j = 0; j < n; ++j) rank += (cost[j] > ci) || (cost[j] == ci && j < i);
-    order[rank] = i;
-  }
-  __syncthreads();
-  // tree mask: item k is tile k % tiles of pair order[k / tiles] (all tiles of a pair
-  // cost the same); causal mask: a tile's keys end at its last row, so items go tile by
-  // tile from the last (longest) tile down, the pairs of each tile longest first
-  for (int k = threadIdx.x; k < n_items; k += blockDim.x) {
-    int q, t;
-    if (causal) {
-      q = k % n;
-      t = tiles - 1 - k / n;
-    } else {
-      q = k / tiles;
-      t = k - q * tiles;
-    }
-    const int pair = ranked ? order[q] : q;
-    const int b = pair / splits;
-    info[k] = make_int4(b, pair - b * splits, t, prefix_len[b]);
-  }
+  schedule(sa);
 }
 
 // ---- host side -----------------------------------------------------------------------
@@ -1229,81 +1499,65 @@ bool tc_supported(const tv_attn_args* a) {
 TcPlan tc_plan(const tv_attn_args* a) {
   TcPlan p{};
   const int clusters = max_clusters() > 0 ? max_clusters() : 74;
-  p.clusters = clusters;
+  p.clusters = std::min(clusters, kMaxSchedClusters);
   p.tiles_per_seq = (a->Q * a->H + kRows - 1) / kRows;
-  const int64_t tiles = (int64_t)a->B * p.tiles_per_seq;
-  const int64_t kv_max = (int64_t)a->max_prefix_len + a->Q;
-  int splits = a->num_splits;
-  if (splits <= 0 && tiles < clusters) {
-    // Fewer tiles than clusters: split the keys.  Pick the count that minimises a simple
-    // makespan model -- items of the longest length dealt to the clusters in rounds, each
-    // costing a tile start-up (about two 128-key steps on this GPU) plus its steps, plus
-    // the combine pass (its HBM bytes at ~6 TB/s, in units of a ~2.4 us step, and one
-    // launch).
-    splits = 1;
-    const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(16, kv_max / 256));
-    const double rows = (double)a->B * a->Q * a->H;
-    double best = 1e30;
-    for (int64_t s = 1; s <= cap; ++s) {
-      const int64_t items = tiles * s;
-      const int64_t rounds = (items + clusters - 1) / clusters;
-      const int64_t steps = ((kv_max + s - 1) / s + kStep - 1) / kStep;
-      const double comb_us = rows * (double)(s + 1) * a->d_latent * 4.0 / 6.0e6;
-      const double t = (double)rounds * (2.0 + (double)steps) + (s > 1 ? 1.0 + comb_us / 2.4 : 0.0);
-      if (t < best - 1e-9) {
-        best = t;
-        splits = (int)s;
-      }
-    }
-  } else if (splits <= 0) {
-    splits = 1;
+  p.n_tiles = (int64_t)a->B * p.tiles_per_seq;
+  p.splits = a->num_splits > 0 ? std::min(a->num_splits, kMaxForcedSplits) : 0;
+  if (p.splits > 0) {
+    p.n_items = p.n_tiles * p.splits;
+    p.max_slots = p.splits > 1 ? p.n_items : 0;
+  } else {
+    // whole tiles, plus at most one piece more per cluster from the quotas; at most two
+    // pieces of split tiles per cluster (its first and its last)
+    p.n_items = p.n_tiles + p.clusters;
+    p.max_slots = 2 * (int64_t)p.clusters;
   }
-  // split boundaries fall on whole 128-key steps
-  int64_t chunk = (kv_max + splits - 1) / splits;
-  chunk = (chunk + kStep - 1) / kStep * kStep;
-  if (chunk < kStep) chunk = kStep;
-  p.chunk = (int)chunk;
-  p.splits = (int)((kv_max + chunk - 1) / chunk);
-  if (p.splits < 1) p.splits = 1;
-  p.n_items = (int)(tiles * p.splits);
   return p;
 }
 
-// Workspace: [work-item records][split partial outputs][split partial lse][paged cache:
-// gathered key view, or per-step tensor maps (2 x 128 B per step) and swap flags].
-size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) {
-  const size_t rows = (size_t)a->B * a->Q * a->H;
-  size_t n = align256((size_t)p.n_items * 16);
-  if (p.splits > 1)
-    n += align256((size_t)p.splits * rows * a->d_latent * 4) + align256((size_t)p.splits * rows * 4);
+// Workspace: [item records: 32 B each][cluster list starts][slot records][partial
+// outputs: slot x 128 x 512 fp32][partial lse][paged
+// cache: gathered key view, or per-step tensor maps (2 x 128 B per step) and swap flags].
+struct TcWs {
+  size_t items, cl_start, slot_info, part_out, part_lse, tail, total;
+};
+TcWs tc_ws_layout(const tv_attn_args* a, const TcPlan& p) {
+  TcWs w{};
+  size_t n = 0;
+  w.items = n;
+  n += align256((size_t)p.n_items * 32);
+  w.cl_start = n;
+  n += align256(((size_t)p.clusters + 2) * 4);
+  w.slot_info = n;
+  n += align256((size_t)p.max_slots * 16);
+  w.part_out = n;
+  n += align256((size_t)p.max_slots * kRows * kDL * 4);
+  w.part_lse = n;
+  n += align256((size_t)p.max_slots * kRows * 4);
+  w.tail = n;
   if (use_gather(a)) {
     n += align256((size_t)a->B * (size_t)gathered_seq_rows(a) * (kDL + kDR) * 2);
   } else if (a->cache.page_table) {
     const size_t steps = (size_t)a->B * (size_t)steps_per_seq(a);
     n += align256(steps * 2 * sizeof(CUtensorMap)) + align256(steps);
   }
-  return n;
+  w.total = n;
+  return w;
 }
 
+size_t tc_workspace(const tv_attn_args* a, const TcPlan& p) { return tc_ws_layout(a, p).total; }
+
 int tc_launch_count(const tv_attn_args* a, const TcPlan& p) {
-  return 2 + (use_gather(a) ? 1 : 0) + (p.splits > 1 ? 1 : 0);
+  return 2 + (use_gather(a) ? 1 : 0) + (p.max_slots > 0 ? 1 : 0);
 }
 
 cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cudaStream_t st) {
   if (!get_encode()) return cudaErrorNotSupported;
   if (max_clusters() <= 0) return cudaErrorNotSupported;
   const size_t rows = (size_t)a->B * a->Q * a->H;
-  char* wsp = (char*)ws;
-  int4* info = (int4*)wsp;
-  wsp += align256((size_t)pl.n_items * 16);
-  float* ws_out = nullptr;
-  float* ws_lse = nullptr;
-  if (pl.splits > 1) {
-    ws_out = (float*)wsp;
-    wsp += align256((size_t)pl.splits * rows * a->d_latent * 4);
-    ws_lse = (float*)wsp;
-    wsp += align256((size_t)pl.splits * rows * 4);
-  }
+  const TcWs lay = tc_ws_layout(a, pl);
+  char* const ws0 = (char*)ws;
+  char* wsp = ws0 + lay.tail;
   const bool gather = use_gather(a);
   const bool paged = a->cache.page_table != nullptr && !gather;  // per-step maps
   const int64_t steps = paged ? steps_per_seq(a) : 0;
@@ -1362,8 +1616,9 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.anc = a->anc;
   p.out = a->out;
   p.lse = a->lse;
-  p.ws_out = ws_out;
-  p.ws_lse = ws_lse;
+  p.ws_out = (float*)(ws0 + lay.part_out);
+  p.ws_lse = (float*)(ws0 + lay.part_lse);
+
   p.status = a->status;
   p.rows_total = (int64_t)rows;
   p.B = a->B;
@@ -1371,10 +1626,8 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   p.Q = a->Q;
   p.max_prefix = a->max_prefix_len;
   p.tiles_per_seq = pl.tiles_per_seq;
-  p.splits = pl.splits;
-  p.chunk = pl.chunk;
-  p.n_items = pl.n_items;
-  p.info = info;
+  p.items = (const int4*)(ws0 + lay.items);
+  p.cl_start = (const int32_t*)(ws0 + lay.cl_start);
   p.step_maps = maps;
   p.step_swap = swap;
   p.page_table = a->cache.page_table;
@@ -1390,16 +1643,33 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     if (g_test_deadline_ns) p.timeout_ns = g_test_deadline_ns;
     p.test_exit_counts = g_test_exit_counts;
   }
-  if (p.n_items == 0) return cudaSuccess;
+  if (pl.n_tiles == 0) return cudaSuccess;
+  // clusters launched: all of them (the quotas spread the work), or with forced splits no
+  // more than there are items
+  const int ncl = (int)std::min<int64_t>(pl.clusters, pl.splits > 0 ? pl.n_items : pl.clusters);
 
   {
+    SchedArgs sa{};
+    sa.prefix_len = a->prefix_len;
+    sa.B = a->B;
+    sa.Q = a->Q;
+    sa.H = a->H;
+    sa.T = pl.tiles_per_seq;
+    sa.causal = p.causal;
+    sa.max_prefix = a->max_prefix_len;
+    sa.seq_cap = seq_cap;
+    sa.ncl = ncl;
+    sa.splits = pl.splits;
+    sa.max_slots = (int)pl.max_slots;
+    sa.items = (int4*)(ws0 + lay.items);
+    sa.cl_start = (int32_t*)(ws0 + lay.cl_start);
+    sa.slot_info = (int4*)(ws0 + lay.slot_info);
+    sa.status = a->status;
     const int64_t map_blocks = paged ? (a->B * steps + 1023) / 1024 : 0;
     prep_kernel<<<(unsigned)(1 + map_blocks), 1024, 0, st>>>(
-        a->prefix_len, a->B, a->Q, pl.splits, pl.chunk, a->max_prefix_len, seq_cap,
-        pl.tiles_per_seq, pl.n_items, info, t_lat, t_rope, (const unsigned char*)a->c_kv,
-        (int64_t)lat_row_bytes * kBN, (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN,
-        a->cache.page_table, a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps, maps,
-        swap, a->mask_mode == TV_MASK_CAUSAL ? 1 : 0, a->status);
+        sa, t_lat, t_rope, (const unsigned char*)a->c_kv, (int64_t)lat_row_bytes * kBN,
+        (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN, a->cache.page_table,
+        a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps, maps, swap);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1413,7 +1683,6 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     if (e != cudaSuccess) return e;
   }
 
-  const int ncl = std::min(pl.clusters, pl.n_items);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * ncl);
   cfg.blockDim = dim3(kThreads);
@@ -1428,11 +1697,13 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  cudaError_t e =
-      cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o, m_q, m_qr);
-  if (e != cudaSuccess || pl.splits == 1) return e;
-  return launch_combine(p.ws_out, p.ws_lse, pl.splits, (int64_t)rows, a->d_latent, a->out,
-                        a->lse, st);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o, m_q, m_qr);
+  if (e != cudaSuccess || pl.max_slots == 0) return e;
+  // merge the pieces of split tiles (blocks of unused slots leave at once)
+  merge_kernel<<<dim3((unsigned)pl.max_slots, kRows / 8), 256, 0, st>>>(
+      (const int4*)(ws0 + lay.slot_info), (const int32_t*)(ws0 + lay.cl_start) + ncl + 1,
+      p.ws_out, p.ws_lse, a->Q * a->H, a->out, a->lse);
+  return cudaGetLastError();
 }
 
 }  // namespace tv

@@ -53,13 +53,15 @@ bool simt_supported(const tv_attn_args* a);
 cudaError_t launch_attn_simt(const tv_attn_args* a, const SimtPlan& p, void* ws,
                              cudaStream_t st);
 
-// Work decomposition of the tensor-core path.
+// Work decomposition of the tensor-core path (the schedule itself is computed on the
+// device from the prefix lengths).
 struct TcPlan {
   int clusters;       // persistent 2-CTA clusters launched (at most)
   int tiles_per_seq;  // ceil(Q*H / 128)
-  int splits;         // KV splits
-  int chunk;          // keys per split (multiple of 64)
-  int n_items;        // B * tiles_per_seq * splits
+  int64_t n_tiles;    // B * tiles_per_seq
+  int splits;         // 0: whole tiles then equal quotas; S > 0: every tile in S pieces
+  int64_t n_items;    // work items at most
+  int64_t max_slots;  // partial-result slots of split tiles at most
 };
 bool tc_supported(const tv_attn_args* a);
 TcPlan tc_plan(const tv_attn_args* a);

@@ -36,16 +36,16 @@ class VerifyStep:
                  "c_kv", "k_pe")
 
     def __init__(self, inp: dict, device="cuda", path=tv.PATH_AUTO, num_splits=0,
-                 paged_view=tv.PAGED_AUTO, causal=False):
+                 paged_view=tv.PAGED_AUTO, causal=None):
         self.inp = inp
         self.device = torch.device(device)
         self.path = path
         self.num_splits = num_splits
         self.paged_view = paged_view
         # causal: prefill of Q tokens after the prefix (no draft tree: no visibility call,
-        # token i at position P + i, the causal mask)
-        self.causal = causal
-        self.mask_mode = tv.MASK_CAUSAL if causal else tv.MASK_TREE
+        # token i at position P + i, the causal mask); by default the workload's own mode
+        self.causal = bool(inp.get("causal", False)) if causal is None else causal
+        self.mask_mode = tv.MASK_CAUSAL if self.causal else tv.MASK_TREE
         d = self.device
         B, Q, H, DL = inp["B"], inp["Q"], inp["H"], inp["DL"]
         self.B, self.Q, self.H, self.DL, self.DR = B, Q, H, DL, inp["DR"]
@@ -59,8 +59,8 @@ class VerifyStep:
         self.c_kv = _dev_float(inp, "c_kv", d)
         self.k_pe = _dev_float(inp, "k_pe", d)
         self.q_pe = torch.zeros_like(self.q_pe_raw)
-        self.anc = None if causal else torch.empty((B, Q), dtype=torch.int64, device=d)
-        self.depth = None if causal else torch.empty((B, Q), dtype=torch.int32, device=d)
+        self.anc = None if self.causal else torch.empty((B, Q), dtype=torch.int64, device=d)
+        self.depth = None if self.causal else torch.empty((B, Q), dtype=torch.int32, device=d)
         self.out = torch.empty((B, Q, H, DL), dtype=torch.float32, device=d)
         self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=d)
         self.status = torch.zeros(1, dtype=torch.int32, device=d)

@@ -42,6 +42,10 @@ WORKLOADS = {
     # B32 H64 q_len 33, chain/random mix, ragged prefix U{4096..8192}, paged, shuffled.
     "cfg5_bf16": dict(B=32, H=64, Q=33, DL=512, DR=64, prefix=(4096, 8192), tree="mix",
                       dtype="bf16", q_var=192.0, scale_den=192.0, paged=True, seed=1005),
+    # Prefill of 4096 tokens with no prior cache (the causal form of the same call).
+    "prefill_bf16": dict(B=1, H=64, Q=4096, DL=512, DR=64, prefix=(0, 0), tree="chain",
+                         dtype="bf16", q_var=192.0, scale_den=192.0, paged=False, seed=1006,
+                         causal=True),
 }
 
 
@@ -145,7 +149,7 @@ def generate(name: str | None = None, seed: int | None = None, **kw) -> dict:
                prefix_len=prefix_len, kv_dtype=cfg["dtype"], q_dtype=cfg["dtype"],
                rope_base=10000.0,
                scale=float(np.float32(1.0 / math.sqrt(cfg["scale_den"]))),
-               tree=cfg["tree"])
+               tree=cfg["tree"], causal=bool(cfg.get("causal", False)))
     arrays = dict(q_latent=q_latent, q_pe=q_pe, kpe_tree=kpe_tree, c_kv=c_kv, k_pe=k_pe)
     for k, v in arrays.items():
         if cfg["dtype"] == "bf16":

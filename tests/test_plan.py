@@ -6,7 +6,8 @@ decided on the host from the argument struct.  These tests check the documented 
   * TV_PATH_AUTO takes the tensor cores for bf16 queries and cache with d_latent 512,
     d_rope 64 and at least 256 (row, head) rows, and the CUDA cores otherwise;
   * a tensor-core call enqueues work preparation + attention, plus a key gather when a
-    paged cache's keys exceed 64 MB, plus a combine when the keys are split;
+    paged cache's keys exceed 64 MB, plus the merge of split tiles unless every tile is
+    forced into one piece;
   * the workspace has room for what the plan keeps there (split partial outputs, the
     gathered key copy), and a call refuses a workspace that is too small or misaligned
     before it launches anything.
@@ -69,39 +70,39 @@ def test_auto_path_by_shape_and_dtype(tvlib):
 
 
 def test_tensor_core_launch_structure(tvlib):
-    # many row tiles and a contiguous cache: preparation + attention
-    assert launches(args(32, 64, 33, 8192)) == 2
-    # a forced split adds the combine
+    # preparation (schedule) + attention + the merge of split tiles; the automatic schedule
+    # may split tiles (decided on the device), a forced single piece per tile never does
+    assert launches(args(32, 64, 33, 8192)) == 3
+    assert launches(args(32, 64, 33, 8192, num_splits=1)) == 2
     assert launches(args(32, 64, 33, 8192, num_splits=3)) == 3
     # a paged cache of 32 x 8225 keys (about 300 MB of keys) adds the key gather
-    assert launches(args(32, 64, 33, 8192, paged=True)) == 3
-    assert launches(args(32, 64, 33, 8192, paged=True, num_splits=2)) == 4
+    assert launches(args(32, 64, 33, 8192, paged=True)) == 4
+    assert launches(args(32, 64, 33, 8192, paged=True, num_splits=1)) == 3
     # a paged cache of 8 x 4105 keys (about 38 MB) keeps per-step tensor maps: no gather
     assert launches(args(8, 64, 9, 4096, paged=True, num_splits=1)) == 2
-
-
-def test_few_row_tiles_split_the_keys(tvlib):
-    # 8 sequences x 5 row tiles cannot fill the GPU's clusters: the plan splits the keys,
-    # which adds the combine kernel
     assert launches(args(8, 64, 9, 4096, paged=True)) == 3
-    # a short prefix is not split (each split would be under two 128-key steps)
-    assert launches(args(8, 64, 9, 100)) == 2
 
 
 def test_workspace_holds_what_the_plan_keeps_there(tvlib):
     rows = 32 * 33 * 64
+    tiles = 32 * 17
     base = workspace(args(32, 64, 33, 8192))
-    assert 0 < base < (1 << 20)                               # work records only
+    # automatic schedule: item records plus partial results for the split pieces of the
+    # equal quotas (at most two per cluster, 74 clusters assumed without a GPU)
+    assert base >= 2 * 74 * 128 * (512 + 1) * 4
+    assert base < 64 << 20
     ws2 = workspace(args(32, 64, 33, 8192, num_splits=2))
     ws4 = workspace(args(32, 64, 33, 8192, num_splits=4))
-    assert ws2 >= 2 * rows * (512 + 1) * 4                    # partial outputs + lse
-    assert ws4 >= 4 * rows * (512 + 1) * 4 and ws4 > ws2
+    assert ws2 >= 2 * tiles * 128 * (512 + 1) * 4 >= 2 * rows * (512 + 1) * 4
+    assert ws4 >= 4 * tiles * 128 * (512 + 1) * 4 and ws4 > ws2
+    one = workspace(args(32, 64, 33, 8192, num_splits=1))
+    assert 0 < one < (1 << 20)                                # records only: no slots
     gathered = workspace(args(32, 64, 33, 8192, paged=True))
     assert gathered >= 32 * 8225 * (512 + 64) * 2             # contiguous key copy
     maps = workspace(args(8, 64, 9, 4096, paged=True, num_splits=1))
     assert maps >= 8 * ((4105 + 127) // 128) * 256            # two 128-byte maps per step
     assert maps < 8 * 4105 * (512 + 64) * 2                   # and no key copy
-    for size in (base, ws2, gathered, maps):
+    for size in (base, ws2, gathered, maps, one):
         assert size % 256 == 0
 
 
@@ -122,11 +123,11 @@ def test_paged_view_forces_either_form(tvlib):
     assert launches(args(**small, paged_view=tv.PAGED_GATHER)) == 3
     assert workspace(args(**small, paged_view=tv.PAGED_GATHER)) >= 8 * 4224 * (512 + 64) * 2
     # large paged cache: gathered by default, per-step maps when forced
-    big = dict(B=32, H=64, Q=33, max_prefix=8192, paged=True)
+    big = dict(B=32, H=64, Q=33, max_prefix=8192, paged=True, num_splits=1)
     assert launches(args(**big)) == 3
     assert launches(args(**big, paged_view=tv.PAGED_STEP_MAPS)) == 2
     assert workspace(args(**big, paged_view=tv.PAGED_STEP_MAPS)) < 32 * 8225 * 1152
     # a contiguous cache ignores the setting
-    assert launches(args(32, 64, 33, 8192, paged_view=tv.PAGED_GATHER)) == 2
+    assert launches(args(32, 64, 33, 8192, paged_view=tv.PAGED_GATHER, num_splits=1)) == 2
     # out-of-range values are argument errors
     assert path(args(**small, paged_view=3)) == tv.TV_ERR_INVALID_ARG

@@ -66,6 +66,7 @@ def _bind(path):
     lib.tro_tree_accept.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.tro_compact_kv.argtypes = [P, i64, P, i64, i32, i32, P, i32, i32, i64, P, P, P, i32,
                                    i32, P]
+    lib.tro_build_tree.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P]
     return lib
 
 
@@ -282,3 +283,21 @@ def compact_kv(c_kv, k_pe, prefix_len, path, accept_len, page_table=None, page_s
                                 _ptr(_c(accept_len, np.int32)), B, Q, _ptr(newp))
     _check(rc, "compact_kv")
     return ck, kp, newp
+
+
+def build_tree(logprobs, tokens, budget, root=None):
+    """Best-first draft tree from per-depth candidates: logprobs, tokens [B, L, K] (sorted
+    descending over K) -> (parent, tokens, depth) int32 [B, budget+1] and score float32."""
+    lp = _c(logprobs, np.float32)
+    tk = _c(tokens, np.int32)
+    B, L, K = lp.shape
+    Q = budget + 1
+    par = np.zeros((B, Q), np.int32)
+    tks = np.zeros((B, Q), np.int32)
+    dep = np.zeros((B, Q), np.int32)
+    sc = np.zeros((B, Q), np.float32)
+    rt = None if root is None else _c(root, np.int32)
+    rc = _load().tro_build_tree(_ptr(lp), _ptr(tk), _ptr(rt), B, L, K, int(budget), _ptr(par),
+                                _ptr(tks), _ptr(dep), _ptr(sc))
+    _check(rc, "build_tree")
+    return par, tks, dep, sc

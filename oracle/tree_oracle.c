@@ -7,6 +7,10 @@
  * use it.  It shares no code, header, table or helper with the CUDA library.
  *
  * Sources (web pages about a native DDTree engine):
+ *   [VERIFY] "The Precision Imperative: Validating Numerical Accuracy in a Custom CUDA
+ *             Attention Kernel", §"The Context: What Led to This Moment": the first custom
+ *             kernel was a GPU best-first tree builder replacing a per-request CPU heapq
+ *             implementation; the draft tree has a budget of nodes.
  *   [RoPE]   "Precision as Correctness: The Float64 RoPE Decision in a Custom CUDA
  *             Inference Engine", §"The Broader Context: A Full Native Engine from
  *             Scratch": the engine wires a greedy
@@ -21,6 +25,15 @@
  *
  * The pages give no formulas for these steps.  The readings taken (each is listed in the
  * design notes):
+ *   - tree building: the drafter proposes, for each depth d = 1..L after the root, K
+ *     candidate tokens with log-probabilities sorted in descending order (the same for
+ *     every path: a block drafter predicts every position at once).  A tree node is a
+ *     path of candidate ranks (r_1, ..., r_d); its score is the float32 sum of
+ *     lp[1][r_1] + ... + lp[d][r_d] accumulated in depth order.  Best-first search pops the
+ *     best candidate from a heap and pushes its K children, until `budget` nodes are taken;
+ *     "best" is the larger score, then the smaller depth, then the lexicographically
+ *     smaller rank path.  Nodes are numbered in the order they are taken (the root is
+ *     node 0), which is topological.
  *   - target token of node i = argmax over the vocabulary of the target model's logits at
  *     node i (the prediction of the token that follows node i); ties go to the smallest
  *     token id.
@@ -39,6 +52,7 @@
  * Build: gcc -O2 -fopenmp -ffp-contract=off -fPIC -shared, together with tv_oracle.c.
  */
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define TRO_OK 0
@@ -163,5 +177,133 @@ int tro_compact_kv(float* c_kv, int64_t ckv_stride, float* k_pe, int64_t kpe_str
     }
     new_prefix_len[b] = (int32_t)(P + 1 + a);
   }
+  return TRO_OK;
+}
+
+
+/* ------------------------------------------------------------------------------------ */
+/* Best-first draft-tree construction.                                                  */
+/* ------------------------------------------------------------------------------------ */
+
+/* A heap candidate: a node not yet taken. */
+typedef struct {
+  float score;    /* float32 sum of its log-probabilities */
+  int depth;      /* 1..L */
+  int rank;       /* candidate rank at its depth */
+  int parent;     /* index (in the output) of its parent node */
+  int path[16];   /* ranks from depth 1 to depth (lexicographic tie break) */
+} tro_cand;
+
+/* 1 if a comes before b: larger score, then smaller depth, then smaller rank path. */
+static int tro_before(const tro_cand* a, const tro_cand* b) {
+  if (a->score != b->score) return a->score > b->score;
+  if (a->depth != b->depth) return a->depth < b->depth;
+  for (int i = 0; i < a->depth; ++i)
+    if (a->path[i] != b->path[i]) return a->path[i] < b->path[i];
+  return 0;
+}
+
+static void tro_swap(tro_cand* a, tro_cand* b) {
+  tro_cand t = *a;
+  *a = *b;
+  *b = t;
+}
+
+/* binary heap with the best candidate at h[0] */
+static void tro_push(tro_cand* h, int* n, const tro_cand* c) {
+  int i = (*n)++;
+  h[i] = *c;
+  while (i > 0 && tro_before(&h[i], &h[(i - 1) / 2])) {
+    tro_swap(&h[i], &h[(i - 1) / 2]);
+    i = (i - 1) / 2;
+  }
+}
+
+static tro_cand tro_pop(tro_cand* h, int* n) {
+  tro_cand top = h[0];
+  h[0] = h[--(*n)];
+  int i = 0;
+  for (;;) {
+    int l = 2 * i + 1, r = l + 1, m = i;
+    if (l < *n && tro_before(&h[l], &h[m])) m = l;
+    if (r < *n && tro_before(&h[r], &h[m])) m = r;
+    if (m == i) break;
+    tro_swap(&h[i], &h[m]);
+    i = m;
+  }
+  return top;
+}
+
+/*
+ * lp     : [B, L, K] float32 log-probabilities, lp[b][d-1][k] for depth d, sorted in
+ *          descending order over k.
+ * tok    : [B, L, K] int32 candidate tokens.
+ * root   : [B] int32 root token (the last accepted token), nullable (then -1).
+ * budget : draft nodes to take (the tree has budget + 1 nodes); at most the number of
+ *          paths of depth 1..L, and at most 63.
+ * parent, tokens, depth : [B, budget+1] int32 out (node 0: -1 / root / 0).
+ * score  : [B, budget+1] float32 out, nullable (node 0: 0).
+ */
+int tro_build_tree(const float* lp, const int32_t* tok, const int32_t* root, int B, int L,
+                   int K, int budget, int32_t* parent, int32_t* tokens, int32_t* depth,
+                   float* score) {
+  if (B < 0 || L < 1 || L > 16 || K < 1 || budget < 0 || budget > 63) return TRO_ERR_INVALID_ARG;
+  double paths = 0.0, level = 1.0;
+  for (int d = 1; d <= L; ++d) {
+    level *= K;
+    paths += level;
+  }
+  if ((double)budget > paths) return TRO_ERR_INVALID_ARG;
+  const int Q = budget + 1;
+  /* every pop pushes at most K candidates */
+  tro_cand* heap = (tro_cand*)malloc(sizeof(tro_cand) * (size_t)(K * (budget + 1) + 1));
+  if (!heap) return TRO_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const float* lpb = lp + (int64_t)b * L * K;
+    const int32_t* tkb = tok + (int64_t)b * L * K;
+    int32_t* par = parent + (int64_t)b * Q;
+    int32_t* tks = tokens + (int64_t)b * Q;
+    int32_t* dep = depth + (int64_t)b * Q;
+    float* sc = score ? score + (int64_t)b * Q : NULL;
+    par[0] = -1;
+    tks[0] = root ? root[b] : -1;
+    dep[0] = 0;
+    if (sc) sc[0] = 0.0f;
+    int n = 0;
+    /* the root is taken: push its children */
+    for (int k = 0; k < K; ++k) {
+      tro_cand c;
+      memset(&c, 0, sizeof(c));
+      c.score = 0.0f + lpb[k];
+      c.depth = 1;
+      c.rank = k;
+      c.parent = 0;
+      c.path[0] = k;
+      tro_push(heap, &n, &c);
+    }
+    for (int i = 1; i < Q; ++i) {
+      if (n == 0) { /* fewer nodes than the budget (cannot happen for a valid budget) */
+        free(heap);
+        return TRO_ERR_INVALID_ARG;
+      }
+      const tro_cand w = tro_pop(heap, &n);
+      par[i] = w.parent;
+      tks[i] = tkb[(int64_t)(w.depth - 1) * K + w.rank];
+      dep[i] = w.depth;
+      if (sc) sc[i] = w.score;
+      if (w.depth < L) {
+        for (int k = 0; k < K; ++k) {
+          tro_cand c = w;
+          c.score = w.score + lpb[(int64_t)w.depth * K + k];
+          c.depth = w.depth + 1;
+          c.rank = k;
+          c.parent = i;
+          c.path[w.depth] = k;
+          tro_push(heap, &n, &c);
+        }
+      }
+    }
+  }
+  free(heap);
   return TRO_OK;
 }

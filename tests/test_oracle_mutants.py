@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_accept as TAC
+from tests import test_oracle_tree_build as TTB
 from tests import test_oracle_attn as TA
 from tests import test_oracle_rope as TR
 from tests import test_oracle_visibility as TV
@@ -71,6 +72,50 @@ TREE_MUTANTS = {
     "compact_skips_k_pe": ("memcpy(k_pe + dst * kpe_stride, k_pe + src * kpe_stride,",
                            "if (0) memcpy(k_pe + dst * kpe_stride, k_pe + src * kpe_stride,"),
 }
+
+# planted mistakes in the best-first tree builder (tree_oracle.c)
+BUILD_MUTANTS = {
+    "ties_deeper_first": ("if (a->depth != b->depth) return a->depth < b->depth;",
+                          "if (a->depth != b->depth) return a->depth > b->depth;"),
+    "ties_path_reversed": ("if (a->path[i] != b->path[i]) return a->path[i] < b->path[i];",
+                           "if (a->path[i] != b->path[i]) return a->path[i] > b->path[i];"),
+    "child_logprob_off_by_one_depth": ("c.score = w.score + lpb[(int64_t)w.depth * K + k];",
+                                       "c.score = w.score + lpb[(int64_t)(w.depth - 1) * K + k];"),
+    "only_first_child": ("        for (int k = 0; k < K; ++k) {\n          tro_cand c = w;",
+                         "        for (int k = 0; k < 1; ++k) {\n          tro_cand c = w;"),
+    "parent_is_grandparent": ("          c.parent = i;", "          c.parent = w.parent;"),
+    "token_from_wrong_depth": ("tks[i] = tkb[(int64_t)(w.depth - 1) * K + w.rank];",
+                               "tks[i] = tkb[(int64_t)(w.depth > 1 ? w.depth - 2 : 0) * K + w.rank];"),
+}
+
+BUILD_PINS = [
+    lambda: TTB.test_brute_force(3, 3, 10), lambda: TTB.test_brute_force(4, 2, 15),
+    TTB.test_ties_follow_depth_then_rank_path, TTB.test_closed_forms, TTB.test_structure,
+    TTB.test_golden_worked_example,
+]
+
+
+@pytest.mark.parametrize("name", sorted(BUILD_MUTANTS))
+def test_build_pins_catch_planted_mistake(name, tmp_path):
+    src = oracle.source_text("tree")
+    old, new = BUILD_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor not found for {name}"
+    path = oracle.compile_variant(src.replace(old, new), str(tmp_path / f"mut_{name}.so"),
+                                  which="tree")
+    failures = 0
+    with oracle.use_library(path):
+        for pin in BUILD_PINS:
+            try:
+                pin()
+            except (AssertionError, oracle.OracleError):
+                failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
+
+
+def test_unmutated_build_oracle_passes_all_pins():
+    for pin in BUILD_PINS:
+        pin()
+
 
 TREE_PINS = [
     TAC.test_argmax_matches_numpy_and_takes_smallest_index_on_ties,

@@ -259,6 +259,33 @@ int tv_verify_attn_noalloc(const tv_attn_args* a, void* stream);
 size_t tv_noalloc_scratch_bytes(void);
 
 /*
+ * tv_build_tree -- best-first draft-tree construction under a node budget.
+ *
+ * [VERIFY] §"The Context: What Led to This Moment": the engine's GPU best-first tree
+ * builder replaces a per-request CPU heapq implementation.  The pages give no formula; the
+ * reading taken here: the drafter proposes, for each depth d = 1..L after the root, K
+ * candidate tokens with log-probabilities sorted in descending order (one list per depth,
+ * shared by every path).  A node is a path of candidate ranks (r_1..r_d) with token
+ * cand_tokens[b,d-1,r_d] and score lp[b,0,r_1] + ... + lp[b,d-1,r_d] (float32, added in
+ * depth order).  The tree is the root plus the `budget` best nodes taken best first --
+ * larger score, then smaller depth, then lexicographically smaller rank path -- numbered
+ * in the order taken (node 0 is the root), so parent[i] < i.
+ *
+ * logprobs    : device [B, L, K] float32, finite, descending over K (a sequence whose
+ *               lists are not sorted gets TV_ERR_INVALID_ARG in *status).
+ * cand_tokens : device [B, L, K] int32.
+ * root_token  : device [B] int32, nullable (node 0's token; -1 when NULL).
+ * parent, tokens : device [B, budget+1] int32 out, the tree as tv_build_visibility and
+ *               tv_tree_accept take it.  depth [B, budget+1] int32 and score [B, budget+1]
+ *               float32 are optional outputs (nullable).
+ * Returns TV_ERR_UNSUPPORTED unless L <= 16, K <= 16, budget <= 63 (the verify kernels'
+ * q_len <= 64), TV_ERR_INVALID_ARG for a budget above the number of possible nodes.
+ */
+int tv_build_tree(const float* logprobs, const int32_t* cand_tokens, const int32_t* root_token,
+                  int B, int L, int K, int budget, int32_t* parent, int32_t* tokens,
+                  int32_t* depth, float* score, int32_t* status, void* stream);
+
+/*
  * tv_tree_accept -- greedy acceptance of a verified draft tree.
  *
  * [RoPE] §"The Broader Context: A Full Native Engine from Scratch" names a greedy

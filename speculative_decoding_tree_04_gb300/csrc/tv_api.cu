@@ -220,6 +220,30 @@ int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void
   return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_verify_attn");
 }
 
+int tv_build_tree(const float* logprobs, const int32_t* cand_tokens, const int32_t* root_token,
+                  int B, int L, int K, int budget, int32_t* parent, int32_t* tokens,
+                  int32_t* depth, float* score, int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (B < 0 || L < 1 || K < 1 || budget < 0)
+    return fail(TV_ERR_INVALID_ARG, "tv_build_tree: bad B/L/K/budget%s");
+  if (L > 16 || K > 16 || budget > 63)
+    return fail(TV_ERR_UNSUPPORTED, "tv_build_tree: needs L <= 16, K <= 16, budget <= 63%s");
+  double paths = 0.0, level = 1.0;
+  for (int d = 1; d <= L; ++d) {
+    level *= K;
+    paths += level;
+  }
+  if ((double)budget > paths)
+    return fail(TV_ERR_INVALID_ARG, "tv_build_tree: budget exceeds the possible nodes%s");
+  if (B == 0) return TV_OK;
+  if (!logprobs || !cand_tokens || !parent || !tokens)
+    return fail(TV_ERR_INVALID_ARG, "tv_build_tree: NULL pointer%s");
+  cudaError_t e = tv::launch_build_tree(logprobs, cand_tokens, root_token, B, L, K, budget,
+                                        parent, tokens, depth, score, status,
+                                        (cudaStream_t)stream);
+  return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_build_tree");
+}
+
 size_t tv_tree_accept_workspace_size(int B, int Q, int64_t vocab) {
   if (B < 0 || Q < 1 || Q > 64 || vocab < 1) return 0;
   return tv::accept_workspace(B, Q, tv::accept_plan(B, Q, vocab, sm_count()));

@@ -94,6 +94,11 @@ cudaError_t launch_compact(void* c_kv, int64_t ckv_stride_bytes, void* k_pe,
                            const int32_t* path, const int32_t* accept_len, int B, int Q,
                            int32_t* new_prefix_len, int32_t* status, cudaStream_t st);
 
+// Best-first draft-tree construction (k_tree.cu).
+cudaError_t launch_build_tree(const float* lp, const int32_t* tok, const int32_t* root, int B,
+                              int L, int K, int budget, int32_t* parent, int32_t* tokens,
+                              int32_t* depth, float* score, int32_t* status, cudaStream_t st);
+
 // Set the thread-local text returned by tv_last_error() (defined in tv_api.cu).
 void set_last_error(const char* msg);
 

@@ -229,3 +229,24 @@ def generate_accept(inp: dict, vocab: int = VOCAB, seed: int | None = None,
         out["logits_bits"] = bf16_bits(logits)
         out["logits"] = bf16_to_f32(out["logits_bits"]).reshape(B, Q, vocab)
     return out
+
+
+def generate_draft(B: int, L: int = 16, K: int = 8, vocab: int = VOCAB, seed: int = 2024,
+                   concentration: float = 0.7, ties: bool = False) -> dict:
+    """Synthetic drafter proposals for best-first tree building: for every sequence and
+    depth d = 1..L, K candidate tokens (distinct, random ids) with log-probabilities taken
+    from a Dirichlet draw over K + 1 outcomes (the last one stands for the rest of the
+    vocabulary), sorted in descending order.  With ``ties`` some neighbouring candidates
+    get equal log-probabilities.  Numbers only: no tree is built here."""
+    r_p, r_t, r_tie = [np.random.default_rng(s) for s in np.random.SeedSequence(seed).spawn(3)]
+    p = r_p.dirichlet(np.full(K + 1, concentration), size=(B, L))[:, :, :K]
+    lp = np.log(np.maximum(p, 1e-30)).astype(np.float32)
+    lp = -np.sort(-lp, axis=-1)
+    if ties:
+        m = r_tie.random((B, L, K - 1)) < 0.2 if K > 1 else np.zeros((B, L, 0), bool)
+        for k in range(1, K):
+            lp[:, :, k] = np.where(m[:, :, k - 1], lp[:, :, k - 1], lp[:, :, k])
+    tok = np.stack([np.stack([r_t.choice(vocab, size=K, replace=False) for _ in range(L)])
+                    for _ in range(B)]).astype(np.int32)
+    root = r_t.integers(0, vocab, size=B).astype(np.int32)
+    return dict(logprobs=np.ascontiguousarray(lp), cand_tokens=tok, root=root, L=L, K=K)

@@ -8,6 +8,7 @@ this module raises.
     build_visibility(parent, anc, depth, dense_mask=None, status=None)
     rope_neox(x, out, prefix_len, depth, base=10000.0, cache=None)
     verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, ...)
+    build_tree(logprobs, cand_tokens, budget, parent, tokens, root=None, depth=None, ...)
     tree_accept(logits, parent, tokens, accept_len, path, new_tokens, target=None, ...)
     compact_kv(c_kv, k_pe, cache, prefix_len, path, accept_len, new_prefix_len, ...)
 """
@@ -94,6 +95,7 @@ def load():
     lib.tv_last_error.restype = ctypes.c_char_p
     lib.tv_version.restype = ctypes.c_int
     lib.tv_testing_set_wait_fault.argtypes = [i32, ctypes.c_uint64, P]
+    lib.tv_build_tree.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P]
     lib.tv_tree_accept_workspace_size.argtypes = [i32, i32, i64]
     lib.tv_tree_accept_workspace_size.restype = ctypes.c_size_t
     lib.tv_tree_accept.argtypes = [P, i32, i64, i64, P, P, i32, i32, P, P, P, P, P, P,
@@ -335,3 +337,20 @@ def compact_kv(c_kv, k_pe, cache: CacheLayout, prefix_len, path, accept_len, new
                               _ptr(prefix_len), _ptr(path), _ptr(accept_len), B, Q,
                               _ptr(new_prefix_len), _ptr(status), _stream(stream))
     _check(rc, "tv_compact_kv")
+
+
+def build_tree(logprobs, cand_tokens, budget, parent, tokens, root=None, depth=None, score=None,
+               status=None, stream=None):
+    """Best-first draft tree: logprobs [B,L,K] float32 (descending over K), cand_tokens
+    [B,L,K] int32 -> parent, tokens [B, budget+1] int32 (depth, score optional)."""
+    _need_cuda(logprobs, cand_tokens, root, parent, tokens, depth, score, status)
+    B, L, K = logprobs.shape
+    for t in (logprobs, cand_tokens, parent, tokens):
+        if not t.is_contiguous():
+            raise ValueError("tv_build_tree takes contiguous tensors")
+    if logprobs.dtype != torch.float32 or cand_tokens.dtype != torch.int32:
+        raise ValueError("logprobs must be float32 and cand_tokens int32")
+    rc = load().tv_build_tree(_ptr(logprobs), _ptr(cand_tokens), _ptr(root), B, L, K,
+                              int(budget), _ptr(parent), _ptr(tokens), _ptr(depth), _ptr(score),
+                              _ptr(status), _stream(stream))
+    _check(rc, "tv_build_tree")

@@ -164,3 +164,20 @@ def test_causal_mask_allows_long_q_without_anc(tvlib):
     # B*Q*H must stay below 2^31
     assert path_of(fake_args(B=1 << 12, Q=1 << 14, H=64, mask_mode=tv.MASK_CAUSAL, anc=None,
                              cache=tv.CacheLayout(None, 64, 0, 1 << 15))) == tv.TV_ERR_UNSUPPORTED
+
+
+def test_build_tree_argument_errors(tvlib):
+    f = tv.load().tv_build_tree
+
+    def call(B=2, L=16, K=8, budget=32):
+        return f(FAKE, FAKE, None, B, L, K, budget, FAKE, FAKE, None, None, None, None)
+
+    assert call(L=17) == tv.TV_ERR_UNSUPPORTED
+    assert call(K=17) == tv.TV_ERR_UNSUPPORTED
+    assert call(budget=64) == tv.TV_ERR_UNSUPPORTED
+    assert call(L=2, K=2, budget=7) == tv.TV_ERR_INVALID_ARG     # only 6 nodes exist
+    assert call(L=0) == tv.TV_ERR_INVALID_ARG
+    assert call(budget=-1) == tv.TV_ERR_INVALID_ARG
+    assert call(B=0) == tv.TV_OK
+    assert f(None, FAKE, None, 2, 16, 8, 32, FAKE, FAKE, None, None, None, None) == \
+        tv.TV_ERR_INVALID_ARG

@@ -6,6 +6,10 @@ Default workload: B=32 sequences, H=64 heads, q_len=33 draft-tree nodes (chain/r
 mix), ragged prefixes U{4096..8192}, d_latent=512, d_rope=64, bf16 latent cache in
 shuffled 64-token pages (synthetic, seeded).  Prints one JSON line.
 
+The step's pre-attention part is one fused launch (tv_verify_prologue: visibility, RoPE of
+the queries, RoPE of the draft keys into the cache, append of the draft latent rows);
+--separate runs tv_build_visibility and two tv_rope_neox calls instead.
+
 Metric: algorithmic attention TFLOP/s of the whole step (visible (row, key) pairs only,
 2*(2*d_latent + d_rope) flops per pair and head), with HBM GB/s and the roofline
 fraction of the attention kernel beside it.  Inputs are resident in HBM when the timed
@@ -311,9 +315,7 @@ def time_steps(step, steps, warmup, eager, flush, dev, barrier, cold=True):
         s0, a0, a1, s1 = ev[k]
         s0.record(stream)
         if graphs is None:
-            step.visibility()
-            step.rope_q()
-            step.rope_k()
+            step.pre()
         else:
             graphs[0].replay()
         a0.record(stream)
@@ -401,6 +403,9 @@ def main():
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 SIMT, 2 tcgen05")
     ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="run visibility and both RoPE calls as separate launches instead of "
+                         "the fused prologue")
     ap.add_argument("--eager", action="store_true",
                     help="time the plain calls instead of replaying CUDA graphs of them")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -442,7 +447,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    step = VerifyStep(inp, device=dev, path=args.path)
+    step = VerifyStep(inp, device=dev, path=args.path, fused=not args.separate)
     path = step.chosen_path()
     flops, byts, pairs = work_of(inp)
     stream = torch.cuda.current_stream(dev)
@@ -526,7 +531,7 @@ def main():
     configs = {}
     for name in [w for w in also.split(",") if w]:
         inp2 = synth.generate(name)
-        st2 = VerifyStep(inp2, device=dev, path=args.path)
+        st2 = VerifyStep(inp2, device=dev, path=args.path, fused=not args.separate)
         p2 = st2.chosen_path()
         fl2, by2, _ = work_of(inp2)
         ms2, ams2, _ = time_steps(st2, args.steps, args.warmup, args.eager, flush, dev, barrier)
@@ -584,8 +589,10 @@ def main():
                    if args.workload == "cfg5_bf16" else f"mean {float(inp['prefix_len'].mean()):.0f}",
                    "paged": inp["page_table"] is not None, "path": ["auto", "simt", "tcgen05"][path],
                    "l2": "256 MB buffer written between steps (cold L2); per-step CUDA events",
-                   "launch": "eager calls" if args.eager else
-                   "CUDA graphs of the calls (visibility+RoPE, attention), captured once",
+                   "launch": ("eager calls" if args.eager else
+                              "CUDA graphs of the calls (pre-attention, attention), captured once")
+                   + ("; visibility + RoPE + cache append as one fused prologue launch"
+                      if not args.separate else "; visibility and RoPE as separate launches"),
                    "e2e_launch": "eager calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_gbs": attn_gbs,

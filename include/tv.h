@@ -259,6 +259,44 @@ int tv_verify_attn_noalloc(const tv_attn_args* a, void* stream);
 size_t tv_noalloc_scratch_bytes(void);
 
 /*
+ * tv_verify_prologue -- the steps before tv_verify_attn in one launch.
+ *
+ * [RoPE] §"The Thinking Process": cos/sin are computed once and reused; [RoPE] §"The
+ * Broader Context: A Full Native Engine from Scratch": the engine manages the KV cache;
+ * [VERIFY] §Context: the visibility mask.  Same results, bit for bit, as
+ *     tv_build_visibility(parent -> anc, depth)
+ *     tv_rope_neox(q_pe_in -> q_pe_out, position prefix_len + depth)
+ *     tv_rope_neox(kpe_tree -> k_pe cache slots prefix_len + i)
+ * plus the copy of the draft tokens' latent rows ckv_tree[b,i,:] into c_kv cache slot
+ * prefix_len[b] + i, with each node's cos/sin computed once for all of them.
+ */
+typedef struct {
+  uint32_t struct_size;      /* sizeof(tv_prologue_args): ABI check */
+  int32_t B, Q, H;           /* Q <= 64 (tree) */
+  int32_t d_latent, d_rope;  /* d_rope % 8 == 0, d_rope <= 512, H * d_rope <= 8192;
+                                d_latent % 8 == 0 */
+  const int32_t* parent;     /* device [B, Q] draft tree */
+  const int32_t* prefix_len; /* device [B] */
+  const void* q_pe_in;       /* device [B, Q, H, d_rope] contiguous, q_dt */
+  void* q_pe_out;            /* same shape and type; may equal q_pe_in */
+  tv_dtype q_dt;
+  const void* kpe_tree;      /* device [B, Q, d_rope] un-rotated draft keys, kv_dt */
+  const void* ckv_tree;      /* device [B, Q, d_latent] draft latent rows, kv_dt; nullable */
+  void* c_kv;                /* cache arrays (kv_dt), rows 16-byte aligned */
+  void* k_pe;
+  tv_dtype kv_dt;
+  int64_t ckv_row_stride, kpe_row_stride; /* elements */
+  tv_cache_layout cache;     /* slots outside it (or beyond num_rows when set) are skipped */
+  uint64_t* anc;             /* device [B, Q] out */
+  int32_t* depth;            /* device [B, Q] out */
+  double rope_base;
+  int32_t* status;           /* device int32, nullable: TV_ERR_INVALID_TREE for a bad tree
+                                (that sequence's rows are left alone) */
+} tv_prologue_args;
+
+int tv_verify_prologue(const tv_prologue_args* a, void* stream);
+
+/*
  * tv_build_tree -- best-first draft-tree construction under a node budget.
  *
  * [VERIFY] §"The Context: What Led to This Moment": the engine's GPU best-first tree

@@ -24,50 +24,13 @@
 #include <algorithm>
 #include <cmath>
 
+#include "rope_math.h"
 #include "tv_internal.h"
 
 namespace tv {
 namespace {
 
-__device__ __forceinline__ float to_float(float v) { return v; }
-__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ void store_float(float* p, float v) { *p = v; }
-__device__ __forceinline__ void store_float(__nv_bfloat16* p, float v) {
-  *p = __float2bfloat16_rn(v);
-}
-
-constexpr int kMaxHalf = 256;  // d_rope <= 512
-
-// cos and sin of one angle: in double, and each split into float hi + lo
-struct CosSin {
-  double c, s;
-  float ch, cl, sh, sl;
-};
-
-// The double-precision recomputation, kept out of line: inlined, the compiler evaluates it
-// unconditionally (predication), which puts five float64-pipe operations on every element.
-__device__ __noinline__ float rot_out_double(float a, float b, double c, double s) {
-  return __double2float_rn(__fma_rn((double)a, c, -__dmul_rn((double)b, s)));
-}
-
-// float32 rounding of a*C - b*S, where C ~ ch + cl ~ c and S ~ sh + sl ~ s (see above)
-__device__ __forceinline__ float rot_out(float a, float b, const CosSin& t) {
-  const float p = __fmul_rn(a, t.ch), ep = __fmaf_rn(a, t.ch, -p);
-  const float q = __fmul_rn(b, t.sh), eq = __fmaf_rn(b, t.sh, -q);
-  const float d = __fsub_rn(p, q);
-  const float bb = __fsub_rn(d, p);  // TwoSum(p, -q): p - q = d + ed exactly
-  const float ed = __fadd_rn(__fsub_rn(p, __fsub_rn(d, bb)), __fsub_rn(-q, bb));
-  const float cross = __fmaf_rn(a, t.cl, -__fmul_rn(b, t.sl));
-  const float tail = __fadd_rn(__fadd_rn(ed, __fsub_rn(ep, eq)), cross);
-  const float y = __fadd_rn(d, tail);
-  if (fabsf(y) >= 0x1p-19f * __fadd_rn(fabsf(p), fabsf(q))) return y;
-  return rot_out_double(a, b, t.c, t.s);
-}
-
-// inverse frequencies 1 / base^(2k / d_rope), k < d_rope / 2
-struct InvFreq {
-  double v[kMaxHalf];
-};
+using namespace rope;
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(128) rope_kernel(const Tin* in, int64_t isr, int64_t ish,
@@ -86,15 +49,7 @@ __global__ void __launch_bounds__(128) rope_kernel(const Tin* in, int64_t isr, i
   const int P = prefix_len[b];
   const int half = D / 2;
   const double pos = (double)P + (double)dep;
-  for (int k = threadIdx.x; k < half; k += blockDim.x) {
-    CosSin t;
-    sincos(__dmul_rn(pos, inv.v[k]), &t.s, &t.c);
-    t.ch = __double2float_rn(t.c);
-    t.cl = __double2float_rn(__dsub_rn(t.c, (double)t.ch));
-    t.sh = __double2float_rn(t.s);
-    t.sl = __double2float_rn(__dsub_rn(t.s, (double)t.sh));
-    cs[k] = t;
-  }
+  for (int k = threadIdx.x; k < half; k += blockDim.x) cs[k] = make_cossin(__dmul_rn(pos, inv.v[k]));
   __syncthreads();
   int64_t orow = r;
   if (use_cache) {

@@ -220,6 +220,39 @@ int tv_verify_attn(const tv_attn_args* a, void* workspace, size_t ws_bytes, void
   return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_verify_attn");
 }
 
+int tv_verify_prologue(const tv_prologue_args* a, void* stream) {
+  g_last_error.clear();
+  if (!a) return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: args is NULL%s");
+  if (a->struct_size != sizeof(tv_prologue_args))
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: struct_size mismatch (ABI)%s");
+  if (a->B < 0 || a->Q < 1 || a->H < 1 || a->d_rope <= 0 || a->d_latent < 0)
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: bad B/Q/H/d_rope/d_latent%s");
+  if (a->Q > 64) return fail(TV_ERR_UNSUPPORTED, "tv_verify_prologue: Q > 64 not supported%s");
+  if (a->d_rope % 8 || a->d_rope > 512 || a->d_latent % 8)
+    return fail(TV_ERR_UNSUPPORTED, "tv_verify_prologue: d_rope and d_latent must be multiples of 8, d_rope <= 512%s");
+  if ((int64_t)a->H * a->d_rope > 8192)
+    return fail(TV_ERR_UNSUPPORTED, "tv_verify_prologue: H * d_rope must be at most 8192%s");
+  if (!(a->q_dt == TV_F32 || a->q_dt == TV_BF16) || !(a->kv_dt == TV_F32 || a->kv_dt == TV_BF16))
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: bad dtype%s");
+  if (!(a->rope_base > 0.0)) return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: rope_base must be > 0%s");
+  if (a->B == 0) return TV_OK;
+  if (!a->parent || !a->prefix_len || !a->q_pe_in || !a->q_pe_out || !a->kpe_tree || !a->k_pe ||
+      !a->anc || !a->depth || (a->ckv_tree && !a->c_kv))
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: NULL pointer%s");
+  const int64_t ek = a->kv_dt == TV_BF16 ? 2 : 4;
+  if (!aligned16(a->q_pe_in) || !aligned16(a->q_pe_out) || !aligned16(a->kpe_tree) ||
+      !aligned16(a->k_pe) || (a->kpe_row_stride * ek) % 16 || a->kpe_row_stride < a->d_rope ||
+      (a->ckv_tree && (!aligned16(a->ckv_tree) || !aligned16(a->c_kv) ||
+                       (a->ckv_row_stride * ek) % 16 || a->ckv_row_stride < a->d_latent)))
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: tensors and rows must be 16-byte aligned%s");
+  if (a->cache.page_table && (a->cache.page_size <= 0 || a->cache.max_pages <= 0))
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: paged cache needs page_size and max_pages%s");
+  if (!a->cache.page_table && a->cache.kv_stride_b < a->Q)
+    return fail(TV_ERR_INVALID_ARG, "tv_verify_prologue: kv_stride_b too small%s");
+  cudaError_t e = tv::launch_prologue(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? TV_OK : cuda_fail(e, "tv_verify_prologue");
+}
+
 int tv_build_tree(const float* logprobs, const int32_t* cand_tokens, const int32_t* root_token,
                   int B, int L, int K, int budget, int32_t* parent, int32_t* tokens,
                   int32_t* depth, float* score, int32_t* status, void* stream) {

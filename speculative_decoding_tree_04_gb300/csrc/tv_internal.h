@@ -94,6 +94,9 @@ cudaError_t launch_compact(void* c_kv, int64_t ckv_stride_bytes, void* k_pe,
                            const int32_t* path, const int32_t* accept_len, int B, int Q,
                            int32_t* new_prefix_len, int32_t* status, cudaStream_t st);
 
+// The fused steps before the attention (k_prologue.cu).
+cudaError_t launch_prologue(const tv_prologue_args* a, cudaStream_t st);
+
 // Best-first draft-tree construction (k_tree.cu).
 cudaError_t launch_build_tree(const float* lp, const int32_t* tok, const int32_t* root, int B,
                               int L, int K, int budget, int32_t* parent, int32_t* tokens,

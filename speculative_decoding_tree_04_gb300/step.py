@@ -36,7 +36,7 @@ class VerifyStep:
                  "c_kv", "k_pe")
 
     def __init__(self, inp: dict, device="cuda", path=tv.PATH_AUTO, num_splits=0,
-                 paged_view=tv.PAGED_AUTO, causal=None):
+                 paged_view=tv.PAGED_AUTO, causal=None, fused=False):
         self.inp = inp
         self.device = torch.device(device)
         self.path = path
@@ -46,6 +46,9 @@ class VerifyStep:
         # token i at position P + i, the causal mask); by default the workload's own mode
         self.causal = bool(inp.get("causal", False)) if causal is None else causal
         self.mask_mode = tv.MASK_CAUSAL if self.causal else tv.MASK_TREE
+        # fused: visibility, both RoPE calls and the append of the draft latent rows as one
+        # tv_verify_prologue launch (tree steps only)
+        self.fused = bool(fused) and not self.causal
         d = self.device
         B, Q, H, DL = inp["B"], inp["Q"], inp["H"], inp["DL"]
         self.B, self.Q, self.H, self.DL, self.DR = B, Q, H, DL, inp["DR"]
@@ -56,6 +59,7 @@ class VerifyStep:
         self.q_latent = _dev_float(inp, "q_latent", d)
         self.q_pe_raw = _dev_float(inp, "q_pe", d)
         self.kpe_tree = _dev_float(inp, "kpe_tree", d)
+        self.ckv_tree = _dev_float(inp, "ckv_tree", d)
         self.c_kv = _dev_float(inp, "c_kv", d)
         self.k_pe = _dev_float(inp, "k_pe", d)
         self.q_pe = torch.zeros_like(self.q_pe_raw)
@@ -65,7 +69,8 @@ class VerifyStep:
         self.lse = torch.empty((B, Q, H), dtype=torch.float32, device=d)
         self.status = torch.zeros(1, dtype=torch.int32, device=d)
         self.max_prefix = int(inp["prefix_len"].max()) if B else 0
-        self.cache = tv.make_cache(self.page_table, inp["page_size"], inp["kv_stride_b"])
+        self.cache = tv.make_cache(self.page_table, inp["page_size"], inp["kv_stride_b"],
+                                   min(self.c_kv.shape[0], self.k_pe.shape[0]))
         self.workspace = None
         self._alloc_workspace()
 
@@ -106,10 +111,23 @@ class VerifyStep:
                        self.status, self.path, self.num_splits, workspace=self.workspace,
                        stream=stream, paged_view=self.paged_view, mask_mode=self.mask_mode)
 
+    def prologue(self, stream=None):
+        tv.verify_prologue(self.parent, self.prefix_len, self.q_pe_raw, self.q_pe,
+                           self.kpe_tree, self.ckv_tree, self.c_kv, self.k_pe, self.cache,
+                           self.anc, self.depth, self.inp["rope_base"], status=self.status,
+                           stream=stream)
+
+    def pre(self, stream=None):
+        """Everything before the attention: one fused launch, or the separate calls."""
+        if self.fused:
+            self.prologue(stream)
+        else:
+            self.visibility(stream)
+            self.rope_q(stream)
+            self.rope_k(stream)
+
     def run(self, stream=None):
-        self.visibility(stream)
-        self.rope_q(stream)
-        self.rope_k(stream)
+        self.pre(stream)
         self.attention(stream)
 
     def capture_graphs(self):
@@ -127,17 +145,16 @@ class VerifyStep:
         torch.cuda.synchronize(self.device)
         g_pre, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_pre):
-            self.visibility()
-            self.rope_q()
-            self.rope_k()
+            self.pre()
         with torch.cuda.graph(g_attn):
             self.attention()
         return g_pre, g_attn
 
     def launches_per_step(self) -> int:
-        """Kernels one run() enqueues: visibility (not for causal prefill), 2 RoPE, and the
-        attention call's own."""
-        return (2 if self.causal else 3) + tv.attn_launches(self.attn_args())
+        """Kernels one run() enqueues: visibility (not for causal prefill) and 2 RoPE, or
+        the fused prologue, and the attention call's own."""
+        pre = 1 if self.fused else (2 if self.causal else 3)
+        return pre + tv.attn_launches(self.attn_args())
 
     # -- results --------------------------------------------------------------------
     def results(self):

@@ -89,7 +89,8 @@ def generate(name: str | None = None, seed: int | None = None, **kw) -> dict:
     the queries; defaults to q_var), scale_den, paged, page size ``page``).  Returns a dict of numpy arrays plus the sizes:
 
       parent [B,Q] int32, prefix_len [B] int32,
-      q_latent [B,Q,H,DL], q_pe [B,Q,H,DR] (un-rotated), kpe_tree [B,Q,DR] (un-rotated)
+      q_latent [B,Q,H,DL], q_pe [B,Q,H,DR] (un-rotated), kpe_tree [B,Q,DR] (un-rotated),
+      ckv_tree [B,Q,DL] (the draft tokens' latent rows, equal to the cache rows at P + i)
       c_kv [rows,DL], k_pe [rows,DR]: the cache (prefix rows and tree latent rows filled,
       every other row finite random data; the tree k_pe rows are written by the verify
       step itself), page_table [B,max_pages] int32 or None, kv_stride_b.
@@ -150,7 +151,17 @@ def generate(name: str | None = None, seed: int | None = None, **kw) -> dict:
                rope_base=10000.0,
                scale=float(np.float32(1.0 / math.sqrt(cfg["scale_den"]))),
                tree=cfg["tree"], causal=bool(cfg.get("causal", False)))
-    arrays = dict(q_latent=q_latent, q_pe=q_pe, kpe_tree=kpe_tree, c_kv=c_kv, k_pe=k_pe)
+    # the draft tokens' latent rows (what the step appends into cache slots P + i): the
+    # rows the cache holds there
+    if cfg["paged"]:
+        jj = prefix_len.astype(np.int64)[:, None] + np.arange(Q)[None, :]
+        rows_tree = page_table[np.arange(B)[:, None], jj // page].astype(np.int64) * page + jj % page
+    else:
+        rows_tree = (np.arange(B)[:, None] * kv_stride_b + prefix_len.astype(np.int64)[:, None]
+                     + np.arange(Q)[None, :])
+    ckv_tree = c_kv[rows_tree]
+    arrays = dict(q_latent=q_latent, q_pe=q_pe, kpe_tree=kpe_tree, c_kv=c_kv, k_pe=k_pe,
+                  ckv_tree=ckv_tree)
     for k, v in arrays.items():
         if cfg["dtype"] == "bf16":
             bits = bf16_bits(v)

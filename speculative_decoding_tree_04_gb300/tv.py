@@ -7,6 +7,7 @@ this module raises.
 
     build_visibility(parent, anc, depth, dense_mask=None, status=None)
     rope_neox(x, out, prefix_len, depth, base=10000.0, cache=None)
+    verify_prologue(parent, prefix_len, q_pe_in, q_pe_out, kpe_tree, ckv_tree, c_kv, k_pe, ...)
     verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, ...)
     build_tree(logprobs, cand_tokens, budget, parent, tokens, root=None, depth=None, ...)
     tree_accept(logits, parent, tokens, accept_len, path, new_tokens, target=None, ...)
@@ -67,6 +68,23 @@ class AttnArgs(ctypes.Structure):
     ]
 
 
+class PrologueArgs(ctypes.Structure):
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("B", ctypes.c_int32), ("Q", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("d_latent", ctypes.c_int32), ("d_rope", ctypes.c_int32),
+        ("parent", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
+        ("q_pe_in", ctypes.c_void_p), ("q_pe_out", ctypes.c_void_p), ("q_dt", ctypes.c_int),
+        ("kpe_tree", ctypes.c_void_p), ("ckv_tree", ctypes.c_void_p),
+        ("c_kv", ctypes.c_void_p), ("k_pe", ctypes.c_void_p), ("kv_dt", ctypes.c_int),
+        ("ckv_row_stride", ctypes.c_int64), ("kpe_row_stride", ctypes.c_int64),
+        ("cache", CacheLayout),
+        ("anc", ctypes.c_void_p), ("depth", ctypes.c_void_p),
+        ("rope_base", ctypes.c_double),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -96,6 +114,7 @@ def load():
     lib.tv_version.restype = ctypes.c_int
     lib.tv_testing_set_wait_fault.argtypes = [i32, ctypes.c_uint64, P]
     lib.tv_build_tree.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P, P]
+    lib.tv_verify_prologue.argtypes = [ctypes.POINTER(PrologueArgs), P]
     lib.tv_tree_accept_workspace_size.argtypes = [i32, i32, i64]
     lib.tv_tree_accept_workspace_size.restype = ctypes.c_size_t
     lib.tv_tree_accept.argtypes = [P, i32, i64, i64, P, P, i32, i32, P, P, P, P, P, P,
@@ -354,3 +373,32 @@ def build_tree(logprobs, cand_tokens, budget, parent, tokens, root=None, depth=N
                               int(budget), _ptr(parent), _ptr(tokens), _ptr(depth), _ptr(score),
                               _ptr(status), _stream(stream))
     _check(rc, "tv_build_tree")
+
+
+def verify_prologue(parent, prefix_len, q_pe_in, q_pe_out, kpe_tree, ckv_tree, c_kv, k_pe,
+                    cache: CacheLayout, anc, depth, base=10000.0, status=None, stream=None):
+    """tv_verify_prologue: visibility, RoPE of q_pe (into q_pe_out, may be q_pe_in), RoPE of
+    the draft keys into their cache slots and the append of the draft latent rows
+    (ckv_tree may be None), in one launch."""
+    _need_cuda(parent, prefix_len, q_pe_in, q_pe_out, kpe_tree, ckv_tree, c_kv, k_pe, anc,
+               depth, status)
+    B, Q, H, DR = q_pe_in.shape
+    for t in (parent, prefix_len, q_pe_in, q_pe_out, kpe_tree, anc, depth):
+        if not t.is_contiguous():
+            raise ValueError("tv_verify_prologue takes contiguous tensors")
+    a = PrologueArgs()
+    a.struct_size = ctypes.sizeof(PrologueArgs)
+    a.B, a.Q, a.H, a.d_rope = B, Q, H, DR
+    a.d_latent = c_kv.shape[1]
+    a.parent, a.prefix_len = parent.data_ptr(), prefix_len.data_ptr()
+    a.q_pe_in, a.q_pe_out, a.q_dt = q_pe_in.data_ptr(), q_pe_out.data_ptr(), _dt(q_pe_in)
+    a.kpe_tree = kpe_tree.data_ptr()
+    a.ckv_tree = None if ckv_tree is None else ckv_tree.data_ptr()
+    a.c_kv, a.k_pe, a.kv_dt = c_kv.data_ptr(), k_pe.data_ptr(), _dt(k_pe)
+    a.ckv_row_stride, a.kpe_row_stride = c_kv.stride(0), k_pe.stride(0)
+    a.cache = cache
+    a.anc, a.depth = anc.data_ptr(), depth.data_ptr()
+    a.rope_base = float(base)
+    a.status = None if status is None else status.data_ptr()
+    rc = load().tv_verify_prologue(ctypes.byref(a), _stream(stream))
+    _check(rc, "tv_verify_prologue")

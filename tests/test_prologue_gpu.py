@@ -1,0 +1,85 @@
+"""The fused verify prologue (tv_verify_prologue) against the separate calls and the oracle.
+
+One launch does the visibility, the RoPE of the queries' rope part, the RoPE of the draft
+keys into their cache slots and the append of the draft tokens' latent rows.  It uses the
+separate calls' arithmetic, so its results must equal theirs bit for bit; the latent
+rows' cache slots are clobbered first, so the append must write them.  The whole fused
+step is then checked against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_tree_04_gb300 import synth, tv
+from speculative_decoding_tree_04_gb300.step import VerifyStep
+from tests.test_parity_gpu import check_step
+
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("tvlib")]
+
+
+def tree_rows(inp):
+    B, Q = inp["B"], inp["Q"]
+    P = inp["prefix_len"].astype(np.int64)
+    jj = P[:, None] + np.arange(Q)[None, :]
+    if inp["page_table"] is not None:
+        pt = inp["page_table"]
+        return pt[np.arange(B)[:, None], jj // 64].astype(np.int64) * 64 + jj % 64
+    return np.arange(B)[:, None] * inp["kv_stride_b"] + jj
+
+
+CASES = [("cfg3_bf16", {}), ("cfg4_bf16", {}), ("cfg1_fp32", {}), ("cfg2_fp32", {}),
+         ("cfg5_bf16", dict(B=4))]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
+def test_fused_prologue_equals_separate_calls(name, kw):
+    inp = synth.generate(name, **kw)
+    sep = VerifyStep(inp)
+    sep.pre()
+    fus = VerifyStep(inp, fused=True)
+    rows = torch.from_numpy(tree_rows(inp).ravel()).cuda()
+    fus.c_kv[rows] = 0                      # the append must restore these
+    fus.k_pe[rows] = 0
+    fus.pre()
+    torch.cuda.synchronize()
+    assert int(fus.status.item()) == 0
+    for a, b in ((sep.anc, fus.anc), (sep.depth, fus.depth), (sep.q_pe, fus.q_pe),
+                 (sep.k_pe, fus.k_pe), (sep.c_kv, fus.c_kv)):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name,kw", [("cfg4_bf16", {}), ("cfg3_fp32", {}),
+                                     ("cfg5_bf16", dict(B=3))])
+def test_fused_step_parity(name, kw):
+    inp = synth.generate(name, **kw)
+    step = VerifyStep(inp, fused=True)
+    rows = torch.from_numpy(tree_rows(inp).ravel()).cuda()
+    step.c_kv[rows] = 0
+    step.run()
+    check_step(inp, step.results(), oracle.tree_verify_step(inp))
+
+
+def test_fused_prologue_invalid_tree_and_graph_replay():
+    inp = synth.generate(B=3, H=8, Q=6, DL=64, DR=16, prefix=(4, 9), seed=3)
+    inp["parent"][1, 3] = 5
+    step = VerifyStep(inp, fused=True)
+    before = step.q_pe.clone()
+    step.pre()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == tv.TV_ERR_INVALID_TREE
+    assert torch.all(step.depth[1] == -1) and torch.all(step.anc[1] == 0)
+    assert torch.equal(step.q_pe[1], before[1])     # the bad sequence is left alone
+    # graph replay of the fused step equals the plain call
+    inp = synth.generate("cfg4_bf16")
+    step = VerifyStep(inp, fused=True)
+    step.run()
+    ref = step.results()
+    g_pre, g_attn = step.capture_graphs()
+    for t in (step.out, step.lse, step.q_pe, step.anc, step.depth):
+        t.zero_()
+    g_pre.replay()
+    g_attn.replay()
+    got = step.results()
+    for k in ("anc", "depth", "q_pe_rot", "k_pe_cache", "out", "lse"):
+        assert np.array_equal(got[k], ref[k]), k

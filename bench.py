@@ -331,6 +331,44 @@ def time_steps(step, steps, warmup, eager, flush, dev, barrier, cold=True):
     return ms, ams, graphs
 
 
+def time_tree_build(args, inp, dev, barrier, pg):
+    """Time tv_build_tree (the best-first draft tree of the workload's size: budget q_len - 1,
+    16 depths x 8 candidates per sequence) replayed from a CUDA graph; the work is a chain of
+    budget warp-wide argmax rounds per sequence, so the figure is a latency."""
+    import torch
+    from speculative_decoding_tree_04_gb300 import synth, tv
+    B, budget = inp["B"], inp["Q"] - 1
+    d = synth.generate_draft(B, 16, 8, seed=inp.get("seed", 1000) + 17)
+    lp = torch.from_numpy(d["logprobs"]).to(dev)
+    tk = torch.from_numpy(d["cand_tokens"]).to(dev)
+    root = torch.from_numpy(d["root"]).to(dev)
+    par = torch.empty((B, budget + 1), dtype=torch.int32, device=dev)
+    tks = torch.empty_like(par)
+    tv.build_tree(lp, tk, budget, par, tks, root=root)        # first call outside capture
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g):
+            tv.build_tree(lp, tk, budget, par, tks, root=root)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    for _ in range(args.warmup):
+        g.replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    barrier()
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    (us,) = max_over_ranks([us], pg, dev)
+    return {"workload": f"{B} sequences, budget {budget}, 16 depths x 8 candidates",
+            "tree_build_us": us, "nodes_per_s": B * budget / (us * 1e-6),
+            "bound": "latency (a chain of budget argmax rounds per sequence)"}
+
+
 def time_post_verify(args, inp, dev, flush, barrier, peaks, pg):
     """Time tv_tree_accept (argmax of every node's logits + the greedy walk) and
     tv_compact_kv on the workload's trees with a 163840-token float32 vocabulary: HBM-bound
@@ -549,9 +587,10 @@ def main():
         torch.cuda.empty_cache()
 
     # ---- post-verify: greedy tree acceptance + KV compaction on the same trees -------
-    post = None
+    post = pre_tree = None
     if args.workload in ("cfg5_bf16", "cfg4_bf16") and args.batch == 0:
         post = time_post_verify(args, inp, dev, flush, barrier, peaks, pg)
+        pre_tree = time_tree_build(args, inp, dev, barrier, pg)
 
     if rank != 0:
         pg.destroy_process_group() if pg is not None else None
@@ -600,6 +639,7 @@ def main():
         "attn_ms_warm_l2": ams_warm,
         "roofline": roof,
         "configs": configs,
+        "tree_build": pre_tree,
         "post_verify": post,
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -252,41 +252,44 @@ __global__ void __launch_bounds__(256) compact_kernel(
     int32_t* __restrict__ new_prefix_len, int batch, int32_t* status) {
   extern __shared__ uint4 buf[];
   __shared__ int64_t src_row[64], dst_row[64];
+  __shared__ unsigned char s_move[64];
   __shared__ int s_n;
   const int b = blockIdx.x;
   const int P = prefix_len[b];
   const int a = accept_len[b];
   const int words = ckv_words + kpe_words;
-  if (threadIdx.x == 0) {
-    int n = 0, bad = (P < 0 || a < 0 || a >= Q) ? 1 : 0;
-    for (int d = 1; !bad && d <= a; ++d) {
-      const int node = path[(int64_t)b * Q + d];
-      if (node < d || node >= Q) {
-        bad = 1;
-        break;
-      }
-      const int64_t js = (int64_t)P + node, jd = (int64_t)P + d;
-      if (cache.page_table && (js / cache.page_size >= cache.max_pages)) {
-        bad = 1;
-        break;
-      }
-      if (!cache.page_table && js >= cache.kv_stride_b) {
-        bad = 1;
-        break;
-      }
+  // every accepted depth d = threadIdx.x + 1 (at most 63) checks its move in parallel
+  const bool ok_seq = !(P < 0 || a < 0 || a >= Q);
+  const int d = threadIdx.x + 1;
+  bool bad = threadIdx.x == 0 && !ok_seq;
+  if (threadIdx.x < 64) s_move[threadIdx.x] = 0;
+  if (ok_seq && d <= a) {
+    const int node = path[(int64_t)b * Q + d];
+    const int64_t js = (int64_t)P + node, jd = (int64_t)P + d;
+    if (node < d || node >= Q ||
+        (cache.page_table ? js / cache.page_size >= cache.max_pages : js >= cache.kv_stride_b)) {
+      bad = true;
+    } else {
       const int64_t rs = cache_row(cache, b, js), rd = cache_row(cache, b, jd);
-      if (rs < 0 || rd < 0 || rs >= num_rows || rd >= num_rows) {
-        bad = 1;
-        break;
-      }
-      if (rs == rd) continue;
-      src_row[n] = rs;
-      dst_row[n] = rd;
-      ++n;
+      bad = rs < 0 || rd < 0 || rs >= num_rows || rd >= num_rows;
+      src_row[threadIdx.x] = rs;
+      dst_row[threadIdx.x] = rd;
+      s_move[threadIdx.x] = !bad && rs != rd;
     }
-    s_n = bad ? 0 : n;
-    if (bad) report(status, TV_ERR_BOUNDS);
-    new_prefix_len[b] = bad ? P : P + 1 + a;
+  }
+  const bool any_bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    if (any_bad) report(status, TV_ERR_BOUNDS);
+    new_prefix_len[b] = any_bad ? P : P + 1 + a;
+    // the rows that move, in depth order
+    int n = 0;
+    for (int e = 0; !any_bad && e < a; ++e)
+      if (s_move[e]) {
+        src_row[n] = src_row[e];
+        dst_row[n] = dst_row[e];
+        ++n;
+      }
+    s_n = n;
   }
   __syncthreads();
   const int n = s_n;

@@ -1030,10 +1030,10 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
 // its keys through L2); with the causal mask a tile's keys end at its last row, so tiles go
 // from the last tile index down, sequences ranked within each.
 //   - Automatic: the first R = floor(tiles / clusters) rounds deal whole tiles, one per
-//     cluster per round, in snake order (rounds alternate direction).  The remaining
-//     tiles' steps are then cut into equal quotas, one per cluster (stream-K): a tile may
-//     end up in several pieces on consecutive clusters.  A quota is at least kMinPiece
-//     steps and cuts no tile into more than kMaxPieces pieces.
+//     cluster per round, in snake order (rounds alternate direction).  The fewer than
+//     `clusters` tiles left over are cut into pieces of about equal length, at most one
+//     piece per cluster: the piece length T is the smallest for which they fit, at least
+//     kMinPiece steps, and no tile is cut into more than kMaxPieces pieces.
 //   - Forced (num_splits = S): every tile in S pieces of equal step counts, the items in
 //     tile order dealt to the clusters in equal contiguous runs.
 // Each cluster's items are stored consecutively (cl_start[c] .. cl_start[c+1]-1;
@@ -1068,65 +1068,29 @@ __device__ __forceinline__ int tile_steps(const SchedArgs& a, int P, int t) {
   return (int)((kend + kStep - 1) / kStep);
 }
 
-// Exclusive prefix sums of val(i), i < n, over the block (1024 threads, warp shuffles):
-// written to out (nullable); returns the total to every thread.
-template <class F>
-__device__ int block_scan(int n, F val, int32_t* out, int* sh) {
-  const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
-  const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) sum += val(i);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) sh[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += v;
-    }
-    sh[32 + lane] = w;  // inclusive totals of warps 0 .. lane
-  }
-  __syncthreads();
-  const int total = sh[32 + (int)(blockDim.x >> 5) - 1];
-  int run = inc - sum + (warp > 0 ? sh[32 + warp - 1] : 0);
-  if (out)
-    for (int i = lo; i < hi; ++i) {
-      out[i] = run;
-      run += val(i);
-    }
-  __syncthreads();
-  return total;
-}
-
 __device__ void schedule(const SchedArgs& a) {
   // All scratch stays in shared memory: fewer tiles remain for the quotas than there are
   // clusters (<= kMaxSchedClusters).
   __shared__ int order[kMaxRanked];
   __shared__ int sp[kMaxRanked];  // prefix length of every sequence (when B <= kMaxRanked)
-  __shared__ int scan[64];
-  __shared__ int cnt[kMaxSchedClusters], first[kMaxSchedClusters];
-  __shared__ int su[kMaxSchedClusters], sbase[kMaxSchedClusters], scl[kMaxSchedClusters + 1];
-  __shared__ int s_max;
+  __shared__ int sc[kMaxRanked];  // its key steps
+  __shared__ int su[kMaxSchedClusters], sbase[kMaxSchedClusters];
+  __shared__ int rs[kMaxSchedClusters], rk[kMaxSchedClusters];
   const int B = a.B, T = a.T, ncl = a.ncl;
   const int n_tiles = B * T;
   const bool ranked = B <= kMaxRanked;
-  for (int i = threadIdx.x; ranked && i < B; i += blockDim.x) sp[i] = a.prefix_len[i];
+  for (int i = threadIdx.x; ranked && i < B; i += blockDim.x) {
+    sp[i] = a.prefix_len[i];
+    sc[i] = tile_steps(a, sp[i], T - 1);
+  }
   __syncthreads();
   auto P_of = [&](int b) { return ranked ? sp[b] : a.prefix_len[b]; };
   // sequences longest first (ties by index); beyond kMaxRanked the identity
   for (int i = threadIdx.x; ranked && i < B; i += blockDim.x) {
-    const int ci = tile_steps(a, sp[i], T - 1);
+    const int ci = sc[i];
     int rank = 0;
     for (int j = 0; j < B; ++j) {
-      const int cj = tile_steps(a, sp[j], T - 1);
+      const int cj = sc[j];
       rank += (cj > ci) || (cj == ci && j < i);
     }
     order[rank] = i;
@@ -1168,45 +1132,68 @@ __device__ void schedule(const SchedArgs& a) {
 
   const int R = n_tiles / ncl;  // rounds of whole tiles
   const int nd = R * ncl;
-  const int nr = n_tiles - nd;  // tiles left for the quotas
-  if (threadIdx.x == 0) s_max = 0;
-  for (int c = threadIdx.x; c < ncl; c += blockDim.x) {
-    cnt[c] = 0;
-    first[c] = 0x7fffffff;
-  }
-  __syncthreads();
-  auto rem_steps = [&](int i) {
-    int b, t;
-    tile_at(nd + i, b, t);
-    return tile_steps(a, P_of(b), t);
-  };
-  const int W = block_scan(nr, rem_steps, su, scan);
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) atomicMax(&s_max, rem_steps(i));
-  __syncthreads();
-  int q = max((W + ncl - 1) / ncl, kMinPiece);
-  q = max(q, (s_max + kMaxPieces - 1) / kMaxPieces);
-  // clusters a remaining tile touches: [c0, c1]
-  auto span = [&](int i, int& c0, int& c1) {
-    const int u = su[i], ns = rem_steps(i);
-    c0 = min(u / q, ncl - 1);
-    c1 = ns > 0 ? min((u + ns - 1) / q, ncl - 1) : c0;
-  };
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-    int c0, c1;
-    span(i, c0, c1);
-    for (int c = c0; c <= c1; ++c) {
-      atomicAdd(&cnt[c], 1);
-      atomicMin(&first[c], i);
+  const int nr = n_tiles - nd;  // tiles left over (fewer than ncl)
+  // The leftover tiles are cut into equal pieces, at most one per cluster: tile i into
+  // k_i = ceil(ns_i / T) pieces (an empty tile: one), with T the smallest piece length for
+  // which the pieces fit the clusters.  T is at least kMinPiece steps and cuts no tile into
+  // more than kMaxPieces pieces.  All of it runs in warp 0 on shared-memory lists (fewer
+  // than ncl leftover tiles).
+  __shared__ int s_pieces, s_slots;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int mx = 0;
+    for (int i = lane; i < nr; i += 32) {
+      int b, t;
+      tile_at(nd + i, b, t);
+      rs[i] = tile_steps(a, P_of(b), t);
+      mx = max(mx, rs[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __syncwarp();
+    auto count = [&](int len) {
+      int c = 0;
+      for (int i = lane; i < nr; i += 32) c += max(1, (rs[i] + len - 1) / len);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      return c;
+    };
+    int lo = max(kMinPiece, (mx + kMaxPieces - 1) / kMaxPieces), hi = max(lo, mx);
+    while (lo < hi) {  // count(hi) <= nr < ncl, so a fitting T exists
+      const int mid = (lo + hi) >> 1;
+      if (count(mid) <= ncl) hi = mid; else lo = mid + 1;
+    }
+    // k_i, first cluster su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time)
+    int run_c = 0, run_s = 0;
+    for (int i0 = 0; i0 < nr; i0 += 32) {
+      const int i = i0 + lane;
+      const int k = i < nr ? max(1, (rs[i] + lo - 1) / lo) : 0;
+      const int ks = k > 1 ? k : 0;
+      int ic = k, is = ks;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vc = __shfl_up_sync(0xffffffffu, ic, o), vs = __shfl_up_sync(0xffffffffu, is, o);
+        if (lane >= o) {
+          ic += vc;
+          is += vs;
+        }
+      }
+      if (i < nr) {
+        su[i] = run_c + ic - k;
+        sbase[i] = run_s + is - ks;
+        rk[i] = k;
+      }
+      run_c += __shfl_sync(0xffffffffu, ic, 31);
+      run_s += __shfl_sync(0xffffffffu, is, 31);
+    }
+    if (lane == 0) {
+      s_pieces = run_c;
+      s_slots = run_s;
     }
   }
   __syncthreads();
-  auto split_slots = [&](int i) {
-    int c0, c1;
-    span(i, c0, c1);
-    return c1 > c0 ? c1 - c0 + 1 : 0;
-  };
-  const int n_slots = block_scan(nr, split_slots, sbase, scan);
-  if (n_slots > a.max_slots) {  // cannot happen (at most two split pieces per cluster)
+  const int n_pieces = s_pieces, n_slots = s_slots;
+  if (n_slots > a.max_slots || n_pieces > ncl) {  // cannot happen (see above)
     if (threadIdx.x == 0) {
       report(a.status, TV_ERR_UNSUPPORTED);
       a.cl_start[ncl + 1] = 0;
@@ -1214,10 +1201,10 @@ __device__ void schedule(const SchedArgs& a) {
     for (int c = threadIdx.x; c <= ncl; c += blockDim.x) a.cl_start[c] = 0;
     return;
   }
-  const int n_items = block_scan(ncl, [&](int c) { return R + cnt[c]; }, scl, scan);
-  for (int c = threadIdx.x; c < ncl; c += blockDim.x) a.cl_start[c] = scl[c];
+  // cluster c: its R whole tiles, then one piece if c < n_pieces
+  for (int c = threadIdx.x; c < ncl; c += blockDim.x) a.cl_start[c] = c * R + min(c, n_pieces);
   if (threadIdx.x == 0) {
-    a.cl_start[ncl] = n_items;
+    a.cl_start[ncl] = nd + n_pieces;
     a.cl_start[ncl + 1] = n_slots;
   }
   // whole tiles of the first R rounds
@@ -1226,18 +1213,17 @@ __device__ void schedule(const SchedArgs& a) {
     const int c = (r & 1) ? ncl - 1 - i : i;
     int b, t;
     tile_at(pos, b, t);
-    put(scl[c] + r, b, t, 0, tile_steps(a, P_of(b), t), 1, -1, -1);
+    put(c * R + min(c, n_pieces) + r, b, t, 0, tile_steps(a, P_of(b), t), 1, -1, -1);
   }
-  // pieces of the remaining tiles
+  // the pieces of the leftover tiles
   for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-    int c0, c1, b, t;
-    span(i, c0, c1);
+    int b, t;
     tile_at(nd + i, b, t);
-    const int u = su[i], ns = rem_steps(i), np = c1 - c0 + 1;
-    for (int c = c0; c <= c1; ++c) {
-      const int s0 = ns > 0 ? max(u, c * q) - u : 0;
-      const int s1 = ns > 0 ? min(u + ns, (c + 1) * q) - u : 0;
-      put(scl[c] + R + (i - first[c]), b, t, s0, s1, np, np > 1 ? sbase[i] + (c - c0) : -1,
+    const int ns = rs[i], np = rk[i];
+    for (int j = 0; j < np; ++j) {
+      const int c = su[i] + j;
+      const int s0 = (int)((int64_t)j * ns / np), s1 = (int)((int64_t)(j + 1) * ns / np);
+      put(c * R + min(c, n_pieces) + R, b, t, s0, s1, np, np > 1 ? sbase[i] + j : -1,
           np > 1 ? sbase[i] : -1);
     }
   }

@@ -455,6 +455,9 @@ def main():
     ap.add_argument("--quick", action="store_true",
                     help="device-timed steps only (no end-to-end pass, no CPU baseline); "
                          "used for profiler runs")
+    ap.add_argument("--parts", action="store_true",
+                    help="with --quick: also time the tree build and the accept + compaction "
+                         "calls (profiler runs of those kernels)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -511,11 +514,16 @@ def main():
     ms, ams = max_over_ranks([ms, ams], pg, dev)
 
     if args.quick:
+        parts = {}
+        if args.parts:
+            parts["tree_build"] = time_tree_build(args, inp, dev, barrier, pg)
+            parts["post_verify"] = time_post_verify(args, inp, dev, flush, barrier,
+                                                    load_peaks(), pg)
         if rank == 0:
             print(json.dumps({"quick": True, "workload": args.workload, "ms_per_step": ms,
                               "attn_ms": ams, "attn_tflops": flops / (ams * 1e-3) / 1e12,
                               "launch": "eager" if graphs is None else "graphs",
-                              "path": ["auto", "simt", "tcgen05"][path]}), flush=True)
+                              "path": ["auto", "simt", "tcgen05"][path], **parts}), flush=True)
         if pg is not None:
             pg.destroy_process_group()
         return

@@ -64,11 +64,11 @@ typedef enum { TV_F32 = 0, TV_BF16 = 1 } tv_dtype;
  * run the request. */
 typedef enum { TV_PATH_AUTO = 0, TV_PATH_SIMT = 1, TV_PATH_TCGEN05 = 2 } tv_path;
 
-/* How the tensor-core path reads a paged cache.  AUTO copies the pages into a contiguous
- * key view in the workspace when the keys exceed 64 MB and builds per-step tensor maps
- * into the pages otherwise; the other two force one form (tests use them to run both
- * forms on small caches).  Ignored by the CUDA-core path and by contiguous caches.
- * TV_PAGED_GATHER needs B * (max_prefix_len + Q rounded up to 128) < 2^31 rows. */
+/* How the tensor-core path reads a paged cache.  AUTO (and TV_PAGED_STEP_MAPS) builds two
+ * tensor maps per 128-key step that read the two 64-token pages of the step in place;
+ * TV_PAGED_GATHER first copies the pages into a contiguous key view in the workspace
+ * (needs B * (max_prefix_len + Q rounded up to 128) < 2^31 rows, else the maps are used).
+ * Ignored by the CUDA-core path and by contiguous caches. */
 typedef enum { TV_PAGED_AUTO = 0, TV_PAGED_STEP_MAPS = 1, TV_PAGED_GATHER = 2 } tv_paged_view;
 
 /* Which keys a query row sees (tv_attn_args.mask_mode).  [GOLDEN] §"Principled

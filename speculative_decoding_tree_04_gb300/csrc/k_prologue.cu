@@ -87,15 +87,21 @@ __device__ __forceinline__ void load_quad(const T* src, int kq, int half, Quad& 
   Vec4<T>::load(src + 4 * kq, q.x0);
   Vec4<T>::load(src + half + 4 * kq, q.x1);
 }
+// The node's cos/sin in shared memory: csf[e * quads + kq] holds the float parts (hi, lo of
+// cos, hi, lo of sin) of frequency 4kq + e -- consecutive quads in consecutive 16-byte slots,
+// so a warp's reads are free of bank conflicts -- and csd[k] the doubles {cos, sin} that
+// only the rare double fallback reads.
 template <typename T>
 __device__ __forceinline__ void rotate_store(const Quad& q, T* dst, int kq, int half,
-                                             const CosSin* cs) {
+                                             const float4* csf, const double2* csd) {
+  const int quads = half / 4;
   float y0[4], y1[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const CosSin t = cs[4 * kq + e];
-    y0[e] = rot_out(q.x0[e], q.x1[e], t);   // x0 cos - x1 sin
-    y1[e] = rot_out(q.x1[e], -q.x0[e], t);  // x1 cos + x0 sin
+    const float4 f = csf[e * quads + kq];
+    const double* dp = &csd[4 * kq + e].x;
+    y0[e] = rot_out_parts(q.x0[e], q.x1[e], f.x, f.y, f.z, f.w, dp);   // x0 cos - x1 sin
+    y1[e] = rot_out_parts(q.x1[e], -q.x0[e], f.x, f.y, f.z, f.w, dp);  // x1 cos + x0 sin
   }
   Vec4<T>::store(dst + 4 * kq, y0);
   Vec4<T>::store(dst + half + 4 * kq, y1);
@@ -106,7 +112,8 @@ constexpr int kQuadsPerThread = 4;  // query quads a thread loads before the ang
 template <typename Tq, typename Tkv>
 __global__ void __launch_bounds__(kThreads, 7) prologue_kernel(const ProParams p,
                                                        const __grid_constant__ InvFreq inv) {
-  __shared__ CosSin cs[kMaxHalf];
+  __shared__ float4 csf[kMaxHalf];
+  __shared__ double2 csd[kMaxHalf];
   __shared__ int s_dep;
   const int i = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,7 +218,11 @@ __global__ void __launch_bounds__(kThreads, 7) prologue_kernel(const ProParams p
   }
   // ---- the node's cos/sin, once, in double ----
   const double pos = (double)P + (double)dep;
-  for (int k = threadIdx.x; k < half; k += blockDim.x) cs[k] = make_cossin(__dmul_rn(pos, inv.v[k]));
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const CosSin t = make_cossin(__dmul_rn(pos, inv.v[k]));
+    csf[(k & 3) * quads + (k >> 2)] = make_float4(t.ch, t.cl, t.sh, t.sl);
+    csd[k] = make_double2(t.c, t.s);
+  }
   __syncthreads();
   // ---- every query head of the node, then the draft key row into its cache slot ----
 #pragma unroll
@@ -219,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 7) prologue_kernel(const ProParams p
     const int idx = threadIdx.x + u * blockDim.x;
     if (idx < nq) {
       const int h = idx / quads;
-      rotate_store<Tq>(qv[u], qo + (int64_t)h * p.DR, idx - h * quads, half, cs);
+      rotate_store<Tq>(qv[u], qo + (int64_t)h * p.DR, idx - h * quads, half, csf, csd);
     }
   }
   // heads beyond what the first pass held (H * d_rope / 8 > 512)
@@ -227,10 +238,10 @@ __global__ void __launch_bounds__(kThreads, 7) prologue_kernel(const ProParams p
     const int h = idx / quads, kq = idx - h * quads;
     Quad x;
     load_quad<Tq>(qi + (int64_t)h * p.DR, kq, half, x);
-    rotate_store<Tq>(x, qo + (int64_t)h * p.DR, kq, half, cs);
+    rotate_store<Tq>(x, qo + (int64_t)h * p.DR, kq, half, csf, csd);
   }
   if (crow >= 0 && (int)threadIdx.x < quads)
-    rotate_store<Tkv>(kv, static_cast<Tkv*>(p.k_pe) + crow * p.kpe_stride, threadIdx.x, half, cs);
+    rotate_store<Tkv>(kv, static_cast<Tkv*>(p.k_pe) + crow * p.kpe_stride, threadIdx.x, half, csf, csd);
 }
 
 }  // namespace

@@ -47,18 +47,24 @@ static __device__ __noinline__ float rot_out_double(float a, float b, double c, 
   return __double2float_rn(__fma_rn((double)a, c, -__dmul_rn((double)b, s)));
 }
 
-// float32 rounding of a*C - b*S, where C ~ ch + cl ~ c and S ~ sh + sl ~ s (see above)
-__device__ __forceinline__ float rot_out(float a, float b, const CosSin& t) {
-  const float p = __fmul_rn(a, t.ch), ep = __fmaf_rn(a, t.ch, -p);
-  const float q = __fmul_rn(b, t.sh), eq = __fmaf_rn(b, t.sh, -q);
+// float32 rounding of a*C - b*S, where C ~ ch + cl ~ c and S ~ sh + sl ~ s (see above);
+// cs points at the double pair {c, s}, read only by the fallback
+__device__ __forceinline__ float rot_out_parts(float a, float b, float ch, float cl, float sh,
+                                               float sl, const double* cs) {
+  const float p = __fmul_rn(a, ch), ep = __fmaf_rn(a, ch, -p);
+  const float q = __fmul_rn(b, sh), eq = __fmaf_rn(b, sh, -q);
   const float d = __fsub_rn(p, q);
   const float bb = __fsub_rn(d, p);  // TwoSum(p, -q): p - q = d + ed exactly
   const float ed = __fadd_rn(__fsub_rn(p, __fsub_rn(d, bb)), __fsub_rn(-q, bb));
-  const float cross = __fmaf_rn(a, t.cl, -__fmul_rn(b, t.sl));
+  const float cross = __fmaf_rn(a, cl, -__fmul_rn(b, sl));
   const float tail = __fadd_rn(__fadd_rn(ed, __fsub_rn(ep, eq)), cross);
   const float y = __fadd_rn(d, tail);
   if (fabsf(y) >= 0x1p-19f * __fadd_rn(fabsf(p), fabsf(q))) return y;
-  return rot_out_double(a, b, t.c, t.s);
+  return rot_out_double(a, b, cs[0], cs[1]);
+}
+
+__device__ __forceinline__ float rot_out(float a, float b, const CosSin& t) {
+  return rot_out_parts(a, b, t.ch, t.cl, t.sh, t.sl, &t.c);
 }
 
 // inverse frequencies 1 / base^(2k / d_rope), k < d_rope / 2 (computed on the host with the

@@ -75,9 +75,12 @@ def test_tensor_core_launch_structure(tvlib):
     assert launches(args(32, 64, 33, 8192)) == 3
     assert launches(args(32, 64, 33, 8192, num_splits=1)) == 2
     assert launches(args(32, 64, 33, 8192, num_splits=3)) == 3
-    # a paged cache of 32 x 8225 keys (about 300 MB of keys) adds the key gather
-    assert launches(args(32, 64, 33, 8192, paged=True)) == 4
-    assert launches(args(32, 64, 33, 8192, paged=True, num_splits=1)) == 3
+    # a paged cache reads its pages in place through per-step tensor maps; the gathered
+    # key view, when asked for, adds the gather
+    assert launches(args(32, 64, 33, 8192, paged=True)) == 3
+    assert launches(args(32, 64, 33, 8192, paged=True, num_splits=1)) == 2
+    assert launches(args(32, 64, 33, 8192, paged=True, num_splits=1,
+                          paged_view=tv.PAGED_GATHER)) == 3
     # a paged cache of 8 x 4105 keys (about 38 MB) keeps per-step tensor maps: no gather
     assert launches(args(8, 64, 9, 4096, paged=True, num_splits=1)) == 2
     assert launches(args(8, 64, 9, 4096, paged=True)) == 3
@@ -97,8 +100,9 @@ def test_workspace_holds_what_the_plan_keeps_there(tvlib):
     assert ws4 >= 4 * tiles * 128 * (512 + 1) * 4 and ws4 > ws2
     one = workspace(args(32, 64, 33, 8192, num_splits=1))
     assert 0 < one < (1 << 20)                                # records only: no slots
-    gathered = workspace(args(32, 64, 33, 8192, paged=True))
+    gathered = workspace(args(32, 64, 33, 8192, paged=True, paged_view=tv.PAGED_GATHER))
     assert gathered >= 32 * 8225 * (512 + 64) * 2             # contiguous key copy
+    assert workspace(args(32, 64, 33, 8192, paged=True)) < gathered
     maps = workspace(args(8, 64, 9, 4096, paged=True, num_splits=1))
     assert maps >= 8 * ((4105 + 127) // 128) * 256            # two 128-byte maps per step
     assert maps < 8 * 4105 * (512 + 64) * 2                   # and no key copy
@@ -122,10 +126,10 @@ def test_paged_view_forces_either_form(tvlib):
     assert launches(args(**small)) == 2
     assert launches(args(**small, paged_view=tv.PAGED_GATHER)) == 3
     assert workspace(args(**small, paged_view=tv.PAGED_GATHER)) >= 8 * 4224 * (512 + 64) * 2
-    # large paged cache: gathered by default, per-step maps when forced
+    # large paged cache: per-step maps by default too, the gathered view when forced
     big = dict(B=32, H=64, Q=33, max_prefix=8192, paged=True, num_splits=1)
-    assert launches(args(**big)) == 3
-    assert launches(args(**big, paged_view=tv.PAGED_STEP_MAPS)) == 2
+    assert launches(args(**big)) == 2
+    assert launches(args(**big, paged_view=tv.PAGED_GATHER)) == 3
     assert workspace(args(**big, paged_view=tv.PAGED_STEP_MAPS)) < 32 * 8225 * 1152
     # a contiguous cache ignores the setting
     assert launches(args(32, 64, 33, 8192, paged_view=tv.PAGED_GATHER, num_splits=1)) == 2

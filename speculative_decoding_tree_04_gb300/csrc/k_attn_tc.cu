@@ -433,6 +433,7 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
             prefetch_tensormap(mn);
             prefetch_tensormap(mn + 1);
           }
+#pragma unroll 1
           for (int h = 0; h < 4; ++h, ++u) {
             const uint32_t st = u % kNLS;
             if (!wait_bar(sh, &sh.slat_empty[st], ((u / kNLS) & 1) ^ 1, p.status)) return;
@@ -500,7 +501,8 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           tc_fence_after();  // the softmax warps' TMEM reads of this S buffer come first
           const uint32_t d = tmem + (sb ? kTmS1 : kTmS0);
           bool ok = true;
-#pragma unroll
+          // (one stage per iteration, not unrolled: see the note on code size in the softmax)
+#pragma unroll 1
           for (int h = 0; h < 4; ++h) {
             if (!wait_bar_cta(sh, &sh.slat_full[st], sph, p.status)) { ok = false; break; }
 #pragma unroll
@@ -614,8 +616,6 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           tmem_ld32(ta + (sw64 ^ 64u), sr + 64);
           tmem_ld32(ta + (sw64 ^ 64u) + 32, sr + 96);
           tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(&sh.s_empty[sb]);
 #pragma unroll
           for (int k = 0; k < 128; ++k) t[k] = __uint_as_float(sr[k]);
         }
@@ -664,8 +664,32 @@ __device__ void s_side(const TcParams& p, const CUtensorMap* map_lat, const CUte
           break;
         }
         unsigned char* stg1 = stg + kMsgBytes;
-        float sum = emit_half(t, c, mr, stg + row_off, sw);
-        if (two) sum += emit_half(t + 64, c, mr, stg1 + row_off, sw);
+        // Code size matters here: the S side's hot loops (producer, MMA issue, softmax) run
+        // on one SM at once, and when they outgrow its instruction cache the misses of all
+        // its SMs queue at the GPC's shared cache (measured: 80 % of that cache's request
+        // rate, 25 % of fetches missing, every SM pair slowed by where it sits in the GPC).
+        // So the two 64-key halves go through one copy of the exponent code, each half's
+        // scores read from tensor memory again (the registers above are only for the max);
+        // the S buffer is released after that second read.
+        float sum = 0.f;
+        {
+          const uint32_t ta = tmem + lane_base + (sb ? kTmS1 : kTmS0);
+#pragma unroll 1
+          for (int hh = 0; hh < (two ? 2 : 1); ++hh) {
+            uint32_t hr[64];
+            float h64[64];
+            const uint32_t col = hh ? (sw64 ^ 64u) : sw64;
+            tmem_ld32(ta + col, hr);
+            tmem_ld32(ta + col + 32, hr + 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 64; ++k) h64[k] = __uint_as_float(hr[k]);
+            apply_mask(h64, hh ? vis1 : vis0);
+            sum += emit_half(h64, c, mr, stg + hh * kMsgBytes + row_off, sw);
+          }
+          tc_fence_before();
+          mbar_arrive(&sh.s_empty[sb]);
+        }
         l = l * alpha + sum;
         reinterpret_cast<float*>(stg + kMsgAlpha)[r] = alpha;
         reinterpret_cast<float*>(stg + kMsgL)[r] = l;

@@ -1068,6 +1068,14 @@ constexpr int kMaxPieces = 8;
 constexpr int kMaxRanked = 1024;
 constexpr int kMaxSchedClusters = 1024;
 constexpr int kMaxForcedSplits = 32;
+// prep_kernel: threads per block (all of them compute the schedule in block 0), threads
+// that write tensor maps in the other blocks, and the shared buffer (block 0: the
+// schedule's lists; the other blocks: two tensor-map copies per map-writing thread)
+constexpr int kPrepThreads = 1024;
+constexpr int kMapThreads = 128;
+constexpr int kPrepSmem = kMapThreads * 2 * 128;
+static_assert(3 * kMaxRanked * 4 + 4 * kMaxSchedClusters * 4 <= kPrepSmem,
+              "the schedule's lists must fit the prep kernel's shared buffer");
 
 struct SchedArgs {
   const int32_t* prefix_len;
@@ -1092,14 +1100,16 @@ __device__ __forceinline__ int tile_steps(const SchedArgs& a, int P, int t) {
   return (int)((kend + kStep - 1) / kStep);
 }
 
-__device__ void schedule(const SchedArgs& a) {
-  // All scratch stays in shared memory: fewer tiles remain for the quotas than there are
-  // clusters (<= kMaxSchedClusters).
-  __shared__ int order[kMaxRanked];
-  __shared__ int sp[kMaxRanked];  // prefix length of every sequence (when B <= kMaxRanked)
-  __shared__ int sc[kMaxRanked];  // its key steps
-  __shared__ int su[kMaxSchedClusters], sbase[kMaxSchedClusters];
-  __shared__ int rs[kMaxSchedClusters], rk[kMaxSchedClusters];
+__device__ void schedule(const SchedArgs& a, unsigned char* buf) {
+  // All scratch stays in shared memory (`buf`): fewer tiles remain for the quotas than
+  // there are clusters (<= kMaxSchedClusters).
+  int* order = reinterpret_cast<int*>(buf);
+  int* sp = order + kMaxRanked;  // prefix length of every sequence (when B <= kMaxRanked)
+  int* sc = sp + kMaxRanked;     // its key steps
+  int* su = sc + kMaxRanked;
+  int* sbase = su + kMaxSchedClusters;
+  int* rs = sbase + kMaxSchedClusters;
+  int* rk = rs + kMaxSchedClusters;
   const int B = a.B, T = a.T, ncl = a.ncl;
   const int n_tiles = B * T;
   const bool ranked = B <= kMaxRanked;
@@ -1310,22 +1320,26 @@ merge_kernel(const int4* __restrict__ slot_info, const int32_t* __restrict__ n_s
 //    step's two tensor maps (latent and rope).  Each is a copy of a host-encoded template
 //    with a new base (the step's lower page), page-dimension stride (distance to its other
 //    page; 0 if both are the same page) and, when the step has one page only, page extent
-//    1 (the missing half reads as zeros).  A page index outside the cache rows is reported
-//    as TV_ERR_BOUNDS and replaced by page 0 (that sequence's result is then undefined, as
-//    for any out-of-range input).
-__global__ void __launch_bounds__(1024)
+//    1 (the missing half reads as zeros).  The fields are edited on a copy in shared
+//    memory (edits of a map in global memory are slow read-modify-writes, and a thread
+//    makes six of them), which is then stored to global memory.  A page index outside the
+//    cache rows is reported as TV_ERR_BOUNDS and replaced by page 0 (that sequence's result
+//    is then undefined, as for any out-of-range input).
+__global__ void __launch_bounds__(kPrepThreads)
 prep_kernel(const SchedArgs sa, const __grid_constant__ CUtensorMap tmpl_lat,
             const __grid_constant__ CUtensorMap tmpl_rope, const unsigned char* ckv,
             int64_t ckv_page_bytes, const unsigned char* kpe, int64_t kpe_page_bytes,
             const int32_t* __restrict__ page_table, int max_pages, int64_t num_pages,
             int steps_per_seq, CUtensorMap* __restrict__ maps, uint8_t* __restrict__ swap) {
+  __shared__ __align__(128) unsigned char buf[kPrepSmem];
   griddep_launch_dependents();  // the attention kernel may start its set-up now
   const int32_t* prefix_len = sa.prefix_len;
   const int B = sa.B, Q = sa.Q, max_prefix = sa.max_prefix;
   const int64_t seq_cap = sa.seq_cap;
   int32_t* status = sa.status;
   if (blockIdx.x > 0) {
-    const int64_t idx = (int64_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+    if (threadIdx.x >= kMapThreads) return;
+    const int64_t idx = (int64_t)(blockIdx.x - 1) * kMapThreads + threadIdx.x;
     if (idx >= (int64_t)B * steps_per_seq) return;
     const int b = (int)(idx / steps_per_seq), sp = (int)(idx - (int64_t)b * steps_per_seq);
     const int P = prefix_len[b];
@@ -1341,29 +1355,35 @@ prep_kernel(const SchedArgs sa, const __grid_constant__ CUtensorMap tmpl_lat,
       pa = pb = 0;
     }
     const int64_t lo = pa < pb ? pa : pb, dist = pa < pb ? pb - pa : pa - pb;
-    CUtensorMap* m = maps + 2 * idx;
+    uint4* sl = reinterpret_cast<uint4*>(buf + threadIdx.x * 256);
+    uint4* sr = sl + 8;
     const uint4* tl = reinterpret_cast<const uint4*>(&tmpl_lat);
     const uint4* tr = reinterpret_cast<const uint4*>(&tmpl_rope);
-    uint4* ml = reinterpret_cast<uint4*>(m);
-    uint4* mr = reinterpret_cast<uint4*>(m + 1);
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      ml[w] = tl[w];
-      mr[w] = tr[w];
+      sl[w] = tl[w];
+      sr[w] = tr[w];
     }
-    tmap_set_address(m, ckv + lo * ckv_page_bytes);
-    tmap_set_stride2(m, (uint64_t)(dist * ckv_page_bytes));
-    tmap_set_address(m + 1, kpe + lo * kpe_page_bytes);
-    tmap_set_stride2(m + 1, (uint64_t)(dist * kpe_page_bytes));
+    const uint32_t al = smem_u32(sl), ar = smem_u32(sr);
+    tmap_set_address_smem(al, ckv + lo * ckv_page_bytes);
+    tmap_set_stride2_smem(al, (uint64_t)(dist * ckv_page_bytes));
+    tmap_set_address_smem(ar, kpe + lo * kpe_page_bytes);
+    tmap_set_stride2_smem(ar, (uint64_t)(dist * kpe_page_bytes));
     if (!has_b) {
-      tmap_set_dim3(m, 1);
-      tmap_set_dim3(m + 1, 1);
+      tmap_set_dim3_smem(al, 1);
+      tmap_set_dim3_smem(ar, 1);
+    }
+    uint4* ml = reinterpret_cast<uint4*>(maps + 2 * idx);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      ml[w] = sl[w];
+      ml[8 + w] = sr[w];
     }
     swap[idx] = (uint8_t)(pb < pa ? 1 : 0);
     tmap_release();
     return;
   }
-  schedule(sa);
+  schedule(sa, buf);
 }
 
 // ---- host side -----------------------------------------------------------------------
@@ -1676,8 +1696,8 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     sa.cl_start = (int32_t*)(ws0 + lay.cl_start);
     sa.slot_info = (int4*)(ws0 + lay.slot_info);
     sa.status = a->status;
-    const int64_t map_blocks = paged ? (a->B * steps + 1023) / 1024 : 0;
-    prep_kernel<<<(unsigned)(1 + map_blocks), 1024, 0, st>>>(
+    const int64_t map_blocks = paged ? (a->B * steps + kMapThreads - 1) / kMapThreads : 0;
+    prep_kernel<<<(unsigned)(1 + map_blocks), kPrepThreads, 0, st>>>(
         sa, t_lat, t_rope, (const unsigned char*)a->c_kv, (int64_t)lat_row_bytes * kBN,
         (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN, a->cache.page_table,
         a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps, maps, swap);

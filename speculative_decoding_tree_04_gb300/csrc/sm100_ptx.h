@@ -46,20 +46,21 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // ---- tensor maps edited on the device ------------------------------------------------
-// A copy of a host-encoded map in global memory gets a new base address, a new byte stride
-// for dimension dim+1 (`dim` indexes the stride array), or a new extent for dimension dim.
-__device__ __forceinline__ void tmap_set_address(void* map, const void* addr) {
-  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(map),
+// A copy of a host-encoded map in this CTA's shared memory (shared-window address) gets a
+// new base address, a new byte stride for dimension 3 (index 2 of the stride array), or a
+// new extent for dimension 3.
+__device__ __forceinline__ void tmap_set_address_smem(uint32_t map, const void* addr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(map),
                "l"((uint64_t)addr)
                : "memory");
 }
-__device__ __forceinline__ void tmap_set_stride2(void* map, uint64_t stride_bytes) {
-  asm volatile("tensormap.replace.tile.global_stride.global.b1024.b64 [%0], 2, %1;" ::"l"(map),
+__device__ __forceinline__ void tmap_set_stride2_smem(uint32_t map, uint64_t stride_bytes) {
+  asm volatile("tensormap.replace.tile.global_stride.shared::cta.b1024.b64 [%0], 2, %1;" ::"r"(map),
                "l"(stride_bytes)
                : "memory");
 }
-__device__ __forceinline__ void tmap_set_dim3(void* map, uint32_t extent) {
-  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 3, %1;" ::"l"(map),
+__device__ __forceinline__ void tmap_set_dim3_smem(uint32_t map, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 3, %1;" ::"r"(map),
                "r"(extent)
                : "memory");
 }

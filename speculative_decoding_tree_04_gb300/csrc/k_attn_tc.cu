@@ -901,12 +901,8 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
           const int rows_ok = p.Q * p.H - wrow0;     // valid rows of the warp's 32
           float* dst0 = dst - (int64_t)lane * kDL;   // row of lane 0
           const int rr4 = lane >> 3, jj = lane & 7;
-#pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            uint32_t v[32];
-            __syncwarp();
-            tmem_ld32(tmem + lane_base + 32 * c, v);
-            tmem_wait_ld();
+          auto put_chunk = [&](const uint32_t* v, int c) {
+            __syncwarp();  // the previous chunk's reads of the staging are done
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               *reinterpret_cast<float4*>(stg + lane * 32 + ((e ^ (lane & 7)) << 2)) =
@@ -920,6 +916,19 @@ __device__ void o_side(const TcParams& p, const CUtensorMap* map_lat, Shared& sh
               if (row < rows_ok)
                 *reinterpret_cast<float4*>(dst0 + (int64_t)row * kDL + 32 * c + 4 * jj) = x;
             }
+          };
+          // two chunks in flight: each TMEM load overlaps the previous chunk's stores
+          uint32_t va[32], vb[32];
+          tmem_ld32(tmem + lane_base, va);
+          tmem_wait_ld_regs(va);
+#pragma unroll 1
+          for (int c = 0; c < 16; c += 2) {
+            tmem_ld32(tmem + lane_base + 32 * (c + 1), vb);
+            put_chunk(va, c);
+            tmem_wait_ld_regs(vb);
+            if (c + 2 < 16) tmem_ld32(tmem + lane_base + 32 * (c + 2), va);
+            put_chunk(vb, c + 1);
+            if (c + 2 < 16) tmem_wait_ld_regs(va);
           }
           tc_fence_before();
           mbar_arrive(&sh.epi_done);

@@ -334,9 +334,19 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 #define TV_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
                  "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define TV_RW8(i) "+r"(r[i + 0]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), \
+                  "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
 #define TV_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
                  "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 
+// Wait for this thread's TMEM loads, with the 32 registers one of them fills as operands:
+// the compiler then keeps every use of them after the wait (a load whose wait comes later,
+// e.g. one issued ahead while the previous chunk is processed, must not be read early).
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : TV_RW8(0), TV_RW8(8), TV_RW8(16), TV_RW8(24)
+               :
+               : "memory");
+}
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base + t).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -354,6 +364,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 #undef TV_R8
+#undef TV_RW8
 #undef TV_W8
 
 }  // namespace ptx

@@ -328,6 +328,24 @@ def time_steps(step, steps, warmup, eager, flush, dev, barrier, cold=True):
     barrier()
     ms = float(np.sum([s0.elapsed_time(s1) for s0, _, _, s1 in ev])) / steps
     ams = float(np.sum([a0.elapsed_time(a1) for _, a0, a1, _ in ev])) / steps
+    if graphs is not None:
+        # The step itself: both parts in one graph, one launch per step (the two-graph
+        # replays above give the attention call's own time).
+        g_step = step.capture_step_graph()
+        for _ in range(warmup):
+            g_step.replay()
+        barrier()
+        ev1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for k in range(steps):
+            if cold:
+                flush.add_(1.0)
+            ev1[k][0].record(stream)
+            g_step.replay()
+            ev1[k][1].record(stream)
+        barrier()
+        ms = float(np.sum([s0.elapsed_time(s1) for s0, s1 in ev1])) / steps
+        graphs = (graphs[0], graphs[1], g_step)
     return ms, ams, graphs
 
 
@@ -500,9 +518,11 @@ def main():
             pg.barrier()
         torch.cuda.synchronize(dev)
 
-    # The timed steps replay two CUDA graphs of the step's calls (captured once; the same
-    # kernels and arguments as the plain calls, without the host's per-call work), unless
-    # --eager asks for the plain calls.
+    # The timed steps replay CUDA graphs of the step's calls (captured once; the same
+    # kernels and arguments as the plain calls, without the host's per-call work): the whole
+    # step as one graph for the step time, and the calls before attention and the attention
+    # call as two graphs for the attention call's own time.  --eager asks for the plain
+    # calls instead.
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)

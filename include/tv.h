@@ -195,12 +195,18 @@ typedef struct {
                                pieces (tensor cores: each 128-row tile's sweep) */
   int32_t paged_view;       /* tv_paged_view; TV_PAGED_AUTO normally */
   int32_t mask_mode;        /* tv_mask_mode; TV_MASK_TREE for tree verification */
+  int32_t overlap_prev;     /* 0 normally.  1: the work queued on the stream before this call
+                               writes none of prefix_len and the page table (as for
+                               tv_verify_prologue, which writes q_pe, cache rows and anc);
+                               the tensor-core path's preparation kernel (work schedule,
+                               per-step tensor maps) may then run while that work finishes.
+                               The attention itself still starts only after all of it. */
 } tv_attn_args;
 
 /* Bytes of workspace tv_verify_attn needs for these arguments (0 if none).  The size
- * depends on B, H, Q, d_latent, max_prefix_len, whether the cache is paged, the path and
- * num_splits only (the tensor-core path of a paged cache also keeps a contiguous copy of
- * the keys there). */
+ * depends on B, H, Q, d_latent, max_prefix_len, whether the cache is paged, the path,
+ * num_splits and paged_view only (the tensor-core path of a paged cache keeps two tensor
+ * maps per 128-key step there, or with TV_PAGED_GATHER a contiguous copy of the keys). */
 size_t tv_verify_attn_workspace_size(const tv_attn_args* a);
 
 /* The kernel family TV_PATH_AUTO resolves to for these arguments, or a negative
@@ -209,9 +215,8 @@ int tv_verify_attn_path(const tv_attn_args* a);
 
 /* How many kernels one tv_verify_attn call with these arguments enqueues (for launch
  * accounting; the CUDA-core path: attention + split combine; the tensor-core path: work
- * preparation + key gather for a large paged cache + attention + the merge of split
- * tiles unless num_splits == 1), or a
- * negative tv_status if the arguments are invalid. */
+ * preparation + key gather (TV_PAGED_GATHER only) + attention + the merge of split tiles
+ * unless num_splits == 1), or a negative tv_status if the arguments are invalid. */
 int tv_verify_attn_launches(const tv_attn_args* a);
 
 /*

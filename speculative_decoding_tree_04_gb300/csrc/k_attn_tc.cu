@@ -1334,14 +1334,12 @@ merge_kernel(const int4* __restrict__ slot_info, const int32_t* __restrict__ n_s
 //    makes six of them), which is then stored to global memory.  A page index outside the
 //    cache rows is reported as TV_ERR_BOUNDS and replaced by page 0 (that sequence's result
 //    is then undefined, as for any out-of-range input).
-__global__ void __launch_bounds__(kPrepThreads)
-prep_kernel(const SchedArgs sa, const __grid_constant__ CUtensorMap tmpl_lat,
-            const __grid_constant__ CUtensorMap tmpl_rope, const unsigned char* ckv,
-            int64_t ckv_page_bytes, const unsigned char* kpe, int64_t kpe_page_bytes,
-            const int32_t* __restrict__ page_table, int max_pages, int64_t num_pages,
-            int steps_per_seq, CUtensorMap* __restrict__ maps, uint8_t* __restrict__ swap) {
-  __shared__ __align__(128) unsigned char buf[kPrepSmem];
-  griddep_launch_dependents();  // the attention kernel may start its set-up now
+__device__ __forceinline__ void prep_body(
+    const SchedArgs& sa, const CUtensorMap& tmpl_lat, const CUtensorMap& tmpl_rope,
+    const unsigned char* ckv, int64_t ckv_page_bytes, const unsigned char* kpe,
+    int64_t kpe_page_bytes, const int32_t* __restrict__ page_table, int max_pages,
+    int64_t num_pages, int steps_per_seq, CUtensorMap* __restrict__ maps,
+    uint8_t* __restrict__ swap, unsigned char* buf) {
   const int32_t* prefix_len = sa.prefix_len;
   const int B = sa.B, Q = sa.Q, max_prefix = sa.max_prefix;
   const int64_t seq_cap = sa.seq_cap;
@@ -1393,6 +1391,24 @@ prep_kernel(const SchedArgs sa, const __grid_constant__ CUtensorMap tmpl_lat,
     return;
   }
   schedule(sa, buf);
+}
+
+// overlap = 0: launched in stream order.  overlap = 1 (tv_attn_args.overlap_prev): launched
+// as a programmatic dependent of the kernel before it, whose outputs it does not read; it
+// does its work while that kernel finishes and waits for it only before leaving, so that
+// the attention kernel's wait on this grid covers both.
+__global__ void __launch_bounds__(kPrepThreads)
+prep_kernel(const SchedArgs sa, const __grid_constant__ CUtensorMap tmpl_lat,
+            const __grid_constant__ CUtensorMap tmpl_rope, const unsigned char* ckv,
+            int64_t ckv_page_bytes, const unsigned char* kpe, int64_t kpe_page_bytes,
+            const int32_t* __restrict__ page_table, int max_pages, int64_t num_pages,
+            int steps_per_seq, CUtensorMap* __restrict__ maps, uint8_t* __restrict__ swap,
+            int overlap) {
+  __shared__ __align__(128) unsigned char buf[kPrepSmem];
+  griddep_launch_dependents();  // the attention kernel may start its set-up now
+  prep_body(sa, tmpl_lat, tmpl_rope, ckv, ckv_page_bytes, kpe, kpe_page_bytes, page_table,
+            max_pages, num_pages, steps_per_seq, maps, swap, buf);
+  if (overlap) griddep_wait();
 }
 
 // ---- host side -----------------------------------------------------------------------
@@ -1706,11 +1722,20 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     sa.slot_info = (int4*)(ws0 + lay.slot_info);
     sa.status = a->status;
     const int64_t map_blocks = paged ? (a->B * steps + kMapThreads - 1) / kMapThreads : 0;
-    prep_kernel<<<(unsigned)(1 + map_blocks), kPrepThreads, 0, st>>>(
-        sa, t_lat, t_rope, (const unsigned char*)a->c_kv, (int64_t)lat_row_bytes * kBN,
-        (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN, a->cache.page_table,
-        a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps, maps, swap);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3((unsigned)(1 + map_blocks));
+    pc.blockDim = dim3(kPrepThreads);
+    pc.stream = st;
+    cudaLaunchAttribute pat[1];
+    pat[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pat[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = pat;
+    pc.numAttrs = a->overlap_prev ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(
+        &pc, prep_kernel, sa, t_lat, t_rope, (const unsigned char*)a->c_kv,
+        (int64_t)lat_row_bytes * kBN, (const unsigned char*)a->k_pe, (int64_t)kpe_row_bytes * kBN,
+        a->cache.page_table, a->cache.max_pages, (int64_t)a->cache.num_rows / kBN, (int)steps,
+        maps, swap, a->overlap_prev ? 1 : 0);
     if (e != cudaSuccess) return e;
   }
   if (gather) {

@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(kThreads, 7) prologue_kernel(const ProParams p
   __shared__ float4 csf[kMaxHalf];
   __shared__ double2 csd[kMaxHalf];
   __shared__ int s_dep;
+  // a programmatic dependent launched after this kernel (the attention call's preparation,
+  // which reads none of this kernel's outputs) may start as soon as every CTA is running
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int i = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Q = p.Q;

@@ -76,8 +76,10 @@ int check_attn(const tv_attn_args* a) {
     return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: kv_stride_b < max_prefix_len + Q%s");
   }
   if (a->path < TV_PATH_AUTO || a->path > TV_PATH_TCGEN05 || a->num_splits < 0 ||
-      a->paged_view < TV_PAGED_AUTO || a->paged_view > TV_PAGED_GATHER)
-    return fail(TV_ERR_INVALID_ARG, "tv_verify_attn: bad path, num_splits or paged_view%s");
+      a->paged_view < TV_PAGED_AUTO || a->paged_view > TV_PAGED_GATHER ||
+      (a->overlap_prev != 0 && a->overlap_prev != 1))
+    return fail(TV_ERR_INVALID_ARG,
+                "tv_verify_attn: bad path, num_splits, paged_view or overlap_prev%s");
   return TV_OK;
 }
 

@@ -104,12 +104,16 @@ class VerifyStep:
         tv.rope_neox(self.kpe_tree, self.k_pe, self.prefix_len, self.depth,
                      self.inp["rope_base"], cache=self.cache, stream=stream)
 
-    def attention(self, stream=None):
+    def attention(self, stream=None, overlap_prev=False):
+        """The attention call.  overlap_prev: the work queued just before it is this step's
+        prologue, which writes neither prefix_len nor the page table, so the call's
+        preparation may overlap it (tv_attn_args.overlap_prev)."""
         tv.verify_attn(self.q_latent, self.q_pe, self.c_kv, self.k_pe, self.prefix_len,
                        self.anc, self.out, self.lse, self.inp["scale"], self.max_prefix,
                        self.page_table, self.inp["page_size"], self.inp["kv_stride_b"],
                        self.status, self.path, self.num_splits, workspace=self.workspace,
-                       stream=stream, paged_view=self.paged_view, mask_mode=self.mask_mode)
+                       stream=stream, paged_view=self.paged_view, mask_mode=self.mask_mode,
+                       overlap_prev=1 if overlap_prev else 0)
 
     def prologue(self, stream=None):
         tv.verify_prologue(self.parent, self.prefix_len, self.q_pe_raw, self.q_pe,
@@ -128,7 +132,7 @@ class VerifyStep:
 
     def run(self, stream=None):
         self.pre(stream)
-        self.attention(stream)
+        self.attention(stream, overlap_prev=self.fused)
 
     def capture_graphs(self):
         """Capture the step as two CUDA graphs: (visibility, both RoPE calls) and the
@@ -149,6 +153,16 @@ class VerifyStep:
         with torch.cuda.graph(g_attn):
             self.attention()
         return g_pre, g_attn
+
+    def capture_step_graph(self):
+        """Capture the whole step (the calls before attention, then the attention call) as
+        one CUDA graph: one launch per step instead of two.  Call after ``capture_graphs``
+        (or ``run``), which does the library's one-time set-up outside any capture."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.pre()
+            self.attention(overlap_prev=self.fused)
+        return g
 
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues: visibility (not for causal prefill) and 2 RoPE, or

@@ -65,6 +65,7 @@ class AttnArgs(ctypes.Structure):
         ("num_splits", ctypes.c_int32),
         ("paged_view", ctypes.c_int32),
         ("mask_mode", ctypes.c_int32),
+        ("overlap_prev", ctypes.c_int32),
     ]
 
 
@@ -223,7 +224,8 @@ def rope_neox(x, out, prefix_len, depth, base=10000.0, cache: CacheLayout | None
 
 def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
               page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
-              num_splits=0, paged_view=PAGED_AUTO, mask_mode=MASK_TREE) -> AttnArgs:
+              num_splits=0, paged_view=PAGED_AUTO, mask_mode=MASK_TREE,
+              overlap_prev=0) -> AttnArgs:
     _need_cuda(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, page_table, status)
     B, Q, H, DL = q_latent.shape
     DR = q_pe.shape[-1]
@@ -249,6 +251,7 @@ def attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_
     a.status = None if status is None else status.data_ptr()
     a.path, a.num_splits, a.paged_view = int(path), int(num_splits), int(paged_view)
     a.mask_mode = int(mask_mode)
+    a.overlap_prev = int(overlap_prev)
     return a
 
 
@@ -288,14 +291,15 @@ def noalloc_scratch_bytes() -> int:
 def verify_attn(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale, max_prefix_len,
                 page_table=None, page_size=64, kv_stride_b=0, status=None, path=PATH_AUTO,
                 num_splits=0, workspace=None, stream=None, paged_view=PAGED_AUTO,
-                mask_mode=MASK_TREE):
+                mask_mode=MASK_TREE, overlap_prev=0):
     """Tree-verify attention; out [B,Q,H,DL] and lse [B,Q,H] (float32) are written.
 
     ``workspace`` (a CUDA uint8 tensor) is allocated through torch and cached per device
-    when not given."""
+    when not given.  ``overlap_prev=1`` declares that the work queued before the call
+    writes neither prefix_len nor the page table (tv_attn_args.overlap_prev)."""
     a = attn_args(q_latent, q_pe, c_kv, k_pe, prefix_len, anc, out, lse, scale,
                   max_prefix_len, page_table, page_size, kv_stride_b, status, path, num_splits,
-                  paged_view, mask_mode)
+                  paged_view, mask_mode, overlap_prev)
     need = workspace_size(a)
     if workspace is None and need > 0:
         key = q_latent.device

@@ -74,6 +74,7 @@ def test_valid_args_resolve_to_a_path(tvlib):
     (dict(cache=tv.CacheLayout(FAKE, 64, 4, 0)), tv.TV_ERR_INVALID_ARG),  # 2065 > 256 rows
     (dict(path=7), tv.TV_ERR_INVALID_ARG),
     (dict(num_splits=-2), tv.TV_ERR_INVALID_ARG),
+    (dict(overlap_prev=2), tv.TV_ERR_INVALID_ARG),
 ])
 def test_attn_argument_errors(tvlib, kw, code):
     assert path_of(fake_args(**kw)) == code

@@ -83,3 +83,34 @@ def test_fused_prologue_invalid_tree_and_graph_replay():
     got = step.results()
     for k in ("anc", "depth", "q_pe_rot", "k_pe_cache", "out", "lse"):
         assert np.array_equal(got[k], ref[k]), k
+    # and so does the whole step as one graph (the preparation overlapping the prologue)
+    g_step = step.capture_step_graph()
+    for t in (step.out, step.lse, step.q_pe, step.anc, step.depth):
+        t.zero_()
+    g_step.replay()
+    got = step.results()
+    for k in ("anc", "depth", "q_pe_rot", "k_pe_cache", "out", "lse"):
+        assert np.array_equal(got[k], ref[k]), k
+
+
+@pytest.mark.parametrize("name,kw", [("cfg4_bf16", {}), ("cfg5_bf16", dict(B=8))])
+def test_overlapped_preparation_equals_stream_order(name, kw):
+    # tv_attn_args.overlap_prev lets the attention call's preparation run while the
+    # prologue finishes; the attention kernel must still see all of the prologue's output.
+    # Fresh query inputs on every round, so a stale read would show.
+    inp = synth.generate(name, **kw)
+    a = VerifyStep(inp, fused=True)
+    b = VerifyStep(inp, fused=True)
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    for _ in range(6):
+        fresh = torch.randn(a.q_pe_raw.shape, generator=gen, device="cuda").to(a.q_pe_raw.dtype)
+        for st in (a, b):
+            st.q_pe_raw.copy_(fresh)
+            st.out.zero_()
+            st.lse.zero_()
+        a.pre()
+        a.attention(overlap_prev=False)
+        b.run()                                   # overlap_prev = 1
+        torch.cuda.synchronize()
+        assert int(b.status.item()) == 0
+        assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)

@@ -48,64 +48,6 @@ struct ProParams {
   int32_t* status;
 };
 
-template <typename T>
-struct Vec4;
-template <>
-struct Vec4<float> {
-  using type = float4;
-  __device__ static void load(const float* p, float* x) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
-  }
-  __device__ static void store(float* p, const float* x) {
-    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-  }
-};
-template <>
-struct Vec4<__nv_bfloat16> {
-  __device__ static void load(const __nv_bfloat16* p, float* x) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    x[0] = __uint_as_float(u.x << 16), x[1] = __uint_as_float(u.x & 0xffff0000u);
-    x[2] = __uint_as_float(u.y << 16), x[3] = __uint_as_float(u.y & 0xffff0000u);
-  }
-  __device__ static void store(__nv_bfloat16* p, const float* x) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
-  }
-};
-
-// Pairs (k, k + half) for k in 4kq .. 4kq+3 of one rope vector: loaded early (before the
-// node's cos/sin exist), rotated and stored later.
-struct Quad {
-  float x0[4], x1[4];
-};
-template <typename T>
-__device__ __forceinline__ void load_quad(const T* src, int kq, int half, Quad& q) {
-  Vec4<T>::load(src + 4 * kq, q.x0);
-  Vec4<T>::load(src + half + 4 * kq, q.x1);
-}
-// The node's cos/sin in shared memory: csf[e * quads + kq] holds the float parts (hi, lo of
-// cos, hi, lo of sin) of frequency 4kq + e -- consecutive quads in consecutive 16-byte slots,
-// so a warp's reads are free of bank conflicts -- and csd[k] the doubles {cos, sin} that
-// only the rare double fallback reads.
-template <typename T>
-__device__ __forceinline__ void rotate_store(const Quad& q, T* dst, int kq, int half,
-                                             const float4* csf, const double2* csd) {
-  const int quads = half / 4;
-  float y0[4], y1[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float4 f = csf[e * quads + kq];
-    const double* dp = &csd[4 * kq + e].x;
-    y0[e] = rot_out_parts(q.x0[e], q.x1[e], f.x, f.y, f.z, f.w, dp);   // x0 cos - x1 sin
-    y1[e] = rot_out_parts(q.x1[e], -q.x0[e], f.x, f.y, f.z, f.w, dp);  // x1 cos + x0 sin
-  }
-  Vec4<T>::store(dst + 4 * kq, y0);
-  Vec4<T>::store(dst + half + 4 * kq, y1);
-}
 constexpr int kThreads = 128;       // small CTAs: one wave of (node, sequence) CTAs
 constexpr int kQuadsPerThread = 4;  // query quads a thread loads before the angles exist
 

@@ -370,3 +370,58 @@ def test_rope_cancelling_inputs(out_dtype):
     mag = np.abs(x[..., :half]) + np.abs(x[..., half:])
     bound = ulp(o, out_dtype) + np.exp2(-50.0) * np.concatenate([mag, mag], axis=-1)
     assert np.all(np.abs(g - o) <= bound), float(np.max(np.abs(g - o) / bound))
+
+
+@pytest.mark.parametrize("in_dt,out_dt", [(torch.float32, torch.float32),
+                                          (torch.bfloat16, torch.bfloat16),
+                                          (torch.float32, torch.bfloat16)])
+def test_rope_vector_and_elementwise_forms_agree(in_dt, out_dt):
+    """tv_rope_neox takes a vector form (four rotate-half pairs per load) when d_rope is a
+    multiple of 8 and the strides are multiples of four elements, and an element-wise form
+    otherwise; both use the same arithmetic, so their results must be the same bits."""
+    torch.manual_seed(5)
+    dev = torch.device("cuda")
+    B, Q, H, D = 3, 9, 64, 64
+    P = torch.randint(0, 5000, (B,), dtype=torch.int32, device=dev)
+    depth = torch.randint(0, Q, (B, Q), dtype=torch.int32, device=dev)
+    x = torch.randn(B, Q, H, D, device=dev).to(in_dt)
+    wide = torch.zeros(B, Q, H, D + 2, device=dev, dtype=in_dt)
+    wide[..., :D] = x
+    xs = wide[..., :D]                       # head stride D + 2: the element-wise form
+    ov = torch.empty(B, Q, H, D, device=dev, dtype=out_dt)
+    os_ = torch.empty_like(ov)
+    tv.rope_neox(x, ov, P, depth)
+    tv.rope_neox(xs, os_, P, depth)
+    torch.cuda.synchronize()
+    assert torch.equal(ov, os_)
+
+
+@pytest.mark.parametrize("in_dt", [torch.float32, torch.bfloat16])
+def test_rope_bf16_store_equals_rounded_float32_result(in_dt):
+    """For bf16 storage the rotation first tries plain float32 arithmetic and keeps it when
+    the bf16 rounding is already decided; otherwise it takes the exact path.  The stored
+    bits must equal the float32 result (the exact path) rounded to bf16, also for inputs
+    built to cancel."""
+    rng = np.random.default_rng(11)
+    dev = torch.device("cuda")
+    B, Q, H, D = 2, 8, 64, 64
+    half = D // 2
+    P = rng.integers(0, 9000, B).astype(np.int32)
+    depth = rng.integers(0, 8, (B, Q)).astype(np.int32)
+    pos = (P[:, None] + depth).astype(np.float64)[:, :, None, None]
+    inv = 1.0 / np.power(10000.0, 2.0 * np.arange(half) / D)
+    c, s = np.cos(pos * inv), np.sin(pos * inv)
+    x0 = rng.standard_normal((B, Q, H, half)).astype(np.float32)
+    x1 = rng.standard_normal((B, Q, H, half)).astype(np.float32)
+    ok = np.abs(s) > 1e-3
+    near = np.where(ok, x0.astype(np.float64) * c / np.where(ok, s, 1.0), x1).astype(np.float32)
+    x1 = np.where((np.arange(H) % 2 == 0)[None, None, :, None], near, x1)
+    x1 = (x1.view(np.int32) + rng.integers(-2, 3, x1.shape).astype(np.int32)).view(np.float32)
+    x = torch.from_numpy(np.concatenate([x0, x1], axis=-1)).to(dev).to(in_dt)
+    Pt, dt = torch.from_numpy(P).to(dev), torch.from_numpy(depth).to(dev)
+    o32 = torch.empty(B, Q, H, D, device=dev, dtype=torch.float32)
+    o16 = torch.empty(B, Q, H, D, device=dev, dtype=torch.bfloat16)
+    tv.rope_neox(x, o32, Pt, dt)
+    tv.rope_neox(x, o16, Pt, dt)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o32.to(torch.bfloat16))

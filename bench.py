@@ -15,10 +15,12 @@ Metric: algorithmic attention TFLOP/s of the whole step (visible (row, key) pair
 fraction of the attention kernel beside it.  Inputs are resident in HBM when the timed
 region starts; between steps a 256 MB buffer is written so that every step starts with
 a cold L2; each step is timed with CUDA events on the launching stream.  The timed steps
-replay two CUDA graphs captured once from the step's calls (visibility + both RoPE calls;
-the attention call), so the same kernels run with the same arguments without the host's
-per-call work; --eager times the plain calls instead.  The end-to-end figure (host
-buffers, copies inside the timed region) always uses the plain calls.
+replay CUDA graphs captured once from the step's calls, so the same kernels run with the
+same arguments without the host's per-call work: the whole step as one graph (its time is
+the step time; the attention call's preparation may overlap the prologue), and the calls
+before attention and the attention call as two graphs (the attention call's own time, the
+roofline's denominator).  --eager times the plain calls instead.  The end-to-end figure
+(host buffers, copies inside the timed region) always uses the plain calls.
 
 --impl reference times the float64 CPU oracle (the repository's own reference
 implementation of the same step) on a bounded sample of the workload per step.
@@ -657,7 +659,8 @@ def main():
                    "paged": inp["page_table"] is not None, "path": ["auto", "simt", "tcgen05"][path],
                    "l2": "256 MB buffer written between steps (cold L2); per-step CUDA events",
                    "launch": ("eager calls" if args.eager else
-                              "CUDA graphs of the calls (pre-attention, attention), captured once")
+                              "the step as one CUDA graph, captured once (attention call timed "
+                              "alone from its own graph)")
                    + ("; visibility + RoPE + cache append as one fused prologue launch"
                       if not args.separate else "; visibility and RoPE as separate launches"),
                    "e2e_launch": "eager calls",

@@ -1302,19 +1302,36 @@ merge_kernel(const int4* __restrict__ slot_info, const int32_t* __restrict__ n_s
   float4 acc[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < np; ++k) {
-    const float wk = __shfl_sync(0xffffffffu, w, k);
-    if (wk == 0.f) continue;  // the same for the whole warp
-    const float4* src = reinterpret_cast<const float4*>(ws_out + ((int64_t)(s + k) * kRows + row) * kDL);
-    float4 v[4];
+  // four pieces' loads in flight at a time (a piece at a time left the warp waiting on
+  // one memory round trip per piece); the products are summed in piece order as before
+  for (int k0 = 0; k0 < np; k0 += 4) {
+    float wk[4];
+    float4 v[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __ldcs(src + lane + 32 * i);
+    for (int q = 0; q < 4; ++q) {
+      const int k = k0 + q;
+      wk[q] = __shfl_sync(0xffffffffu, w, k < np ? k : 0);
+      if (k >= np) wk[q] = 0.f;
+      if (wk[q] != 0.f) {  // the same for the whole warp
+        const float4* src =
+            reinterpret_cast<const float4*>(ws_out + ((int64_t)(s + k) * kRows + row) * kDL);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[i].x = fmaf(wk, v[i].x, acc[i].x);
-      acc[i].y = fmaf(wk, v[i].y, acc[i].y);
-      acc[i].z = fmaf(wk, v[i].z, acc[i].z);
-      acc[i].w = fmaf(wk, v[i].w, acc[i].w);
+        for (int i = 0; i < 4; ++i) v[q][i] = __ldcs(src + lane + 32 * i);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[q][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (wk[q] == 0.f) continue;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i].x = fmaf(wk[q], v[q][i].x, acc[i].x);
+        acc[i].y = fmaf(wk[q], v[q][i].y, acc[i].y);
+        acc[i].z = fmaf(wk[q], v[q][i].z, acc[i].z);
+        acc[i].w = fmaf(wk[q], v[q][i].w, acc[i].w);
+      }
     }
   }
   float4* d4 = reinterpret_cast<float4*>(out + grow * kDL);

@@ -114,3 +114,19 @@ def test_overlapped_preparation_equals_stream_order(name, kw):
         torch.cuda.synchronize()
         assert int(b.status.item()) == 0
         assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+
+
+@pytest.mark.parametrize("name,kw,form", [
+    ("cfg4_bf16", {}, tv.PAGED_GATHER),          # prep -> key gather -> attention
+    ("cfg5_bf16", dict(B=3), tv.PAGED_STEP_MAPS),
+    ("cfg2_fp32", {}, tv.PAGED_AUTO),            # CUDA-core path: no preparation kernel
+])
+def test_overlapped_step_parity_all_forms(name, kw, form):
+    """The step with the attention call's preparation overlapping the prologue
+    (overlap_prev) against the oracle, for each key view and for the CUDA-core path."""
+    inp = synth.generate(name, **kw)
+    step = VerifyStep(inp, fused=True, paged_view=form)
+    rows = torch.from_numpy(tree_rows(inp).ravel()).cuda()
+    step.c_kv[rows] = 0                       # the prologue's append must restore these
+    step.run()
+    check_step(inp, step.results(), oracle.tree_verify_step(inp))

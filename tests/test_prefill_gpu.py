@@ -95,3 +95,32 @@ def test_tree_mode_still_rejects_long_q():
     with pytest.raises(tv.TVError) as e:
         tv.chosen_path(a)
     assert e.value.status == tv.TV_ERR_UNSUPPORTED
+
+
+def test_full_size_prefill_sampled():
+    """The 4096-token, 64-head prefill workload at full size, in the launch configuration
+    the benchmark times; sampled tokens checked against the oracle one by one.  Token i of
+    a prefill from nothing sees keys 0..i, whose k_pe rows were rotated at their own
+    positions: the oracle rebuilds exactly that as a one-node step with a prefix of i keys
+    (the prefix rows rotated by the oracle itself)."""
+    inp = synth.generate("prefill_bf16")
+    step = VerifyStep(inp)
+    step.run()
+    g = step.results()
+    assert g["status"] == 0
+    for i in (0, 1, 63, 64, 127, 128, 1000, 2047, 2048, 4094, 4095):
+        rot = oracle.rope_neox(inp["kpe_tree"][:, :i, None, :], np.zeros(1, np.int32),
+                               np.arange(i, dtype=np.int32)[None, :], inp["rope_base"],
+                               out_bf16=True)[0, :, 0, :]
+        k_pe = np.zeros((i + 1, inp["DR"]), np.float32)
+        k_pe[:i] = rot
+        sub = dict(B=1, Q=1, H=inp["H"], DL=inp["DL"], DR=inp["DR"],
+                   parent=np.full((1, 1), -1, np.int32),
+                   prefix_len=np.full(1, i, np.int32),
+                   q_latent=inp["q_latent"][:, i:i + 1], q_pe=inp["q_pe"][:, i:i + 1],
+                   kpe_tree=inp["kpe_tree"][:, i:i + 1], c_kv=inp["c_kv"][:i + 1], k_pe=k_pe,
+                   page_table=None, page_size=64, kv_stride_b=i + 1, kv_dtype="bf16",
+                   q_dtype="bf16", scale=inp["scale"], rope_base=inp["rope_base"])
+        o = oracle.tree_verify_step(sub)
+        assert_close(g["out"][:, i:i + 1], o["out"], "bf16", f"out token {i}", row_len=inp["DL"])
+        assert_close(g["lse"][:, i:i + 1], o["lse"], "bf16", f"lse token {i}", lse=True)

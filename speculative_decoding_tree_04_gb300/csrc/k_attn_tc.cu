@@ -1179,34 +1179,64 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   // The leftover tiles are cut into equal pieces, at most one per cluster: tile i into
   // k_i = ceil(ns_i / T) pieces (an empty tile: one), with T the smallest piece length for
   // which the pieces fit the clusters.  T is at least kMinPiece steps and cuts no tile into
-  // more than kMaxPieces pieces.  All of it runs in warp 0 on shared-memory lists (fewer
-  // than ncl leftover tiles).
-  __shared__ int s_pieces, s_slots;
+  // more than kMaxPieces pieces.  Every warp tests one candidate length per round (the
+  // piece count falls as the length grows), so two or three rounds find T; warp 0 then
+  // takes the prefix sums (fewer than ncl leftover tiles).
+  __shared__ int s_pieces, s_slots, s_mx, s_lo, s_hi;
+  __shared__ int s_fit[32];
+  if (threadIdx.x == 0) s_mx = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+    int b, t;
+    tile_at(nd + i, b, t);
+    rs[i] = tile_steps(a, P_of(b), t);
+    atomicMax(&s_mx, rs[i]);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int mx = s_mx;
+    s_lo = max(kMinPiece, (mx + kMaxPieces - 1) / kMaxPieces);
+    s_hi = max(s_lo, mx);  // count(hi) <= nr < ncl: hi fits
+  }
+  __syncthreads();
+  {
+    const int nw = min((int)(blockDim.x >> 5), 32), w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (;;) {
+      const int lo = s_lo, hi = s_hi;
+      if (lo >= hi) break;
+      const int stride = (hi - lo + nw - 1) / nw;
+      const int len = lo + w * stride;
+      if (w < nw && len < hi) {
+        int c = 0;
+        for (int i = lane; i < nr; i += 32) c += max(1, (rs[i] + len - 1) / len);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        if (lane == 0) s_fit[w] = c <= ncl ? 1 : 0;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        // candidates in increasing length: the first that fits is the new upper end, the
+        // one before it (which does not) sets the new lower end
+        int nlo = lo, nhi = hi;
+        for (int ww = 0; ww < nw; ++ww) {
+          const int l2 = lo + ww * stride;
+          if (l2 >= hi) break;
+          if (s_fit[ww]) {
+            nhi = l2;
+            break;
+          }
+          nlo = l2 + 1;
+        }
+        s_lo = nlo;
+        s_hi = nhi;
+      }
+      __syncthreads();
+    }
+  }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    int mx = 0;
-    for (int i = lane; i < nr; i += 32) {
-      int b, t;
-      tile_at(nd + i, b, t);
-      rs[i] = tile_steps(a, P_of(b), t);
-      mx = max(mx, rs[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    __syncwarp();
-    auto count = [&](int len) {
-      int c = 0;
-      for (int i = lane; i < nr; i += 32) c += max(1, (rs[i] + len - 1) / len);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-      return c;
-    };
-    int lo = max(kMinPiece, (mx + kMaxPieces - 1) / kMaxPieces), hi = max(lo, mx);
-    while (lo < hi) {  // count(hi) <= nr < ncl, so a fitting T exists
-      const int mid = (lo + hi) >> 1;
-      if (count(mid) <= ncl) hi = mid; else lo = mid + 1;
-    }
-    // k_i, first cluster su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time)
+    const int lo = s_lo;
+    // k_i, first piece su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time)
     int run_c = 0, run_s = 0;
     for (int i0 = 0; i0 < nr; i0 += 32) {
       const int i = i0 + lane;
@@ -1258,17 +1288,21 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
     tile_at(pos, b, t);
     put(c * R + min(c, n_pieces) + r, b, t, 0, tile_steps(a, P_of(b), t), 1, -1, -1);
   }
-  // the pieces of the leftover tiles
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+  // the pieces of the leftover tiles, one thread per piece: piece c (cluster c) belongs
+  // to the last tile i with su[i] <= c
+  for (int c = threadIdx.x; c < n_pieces; c += blockDim.x) {
+    int l = 0, h = nr - 1;
+    while (l < h) {
+      const int m = (l + h + 1) >> 1;
+      if (su[m] <= c) l = m; else h = m - 1;
+    }
+    const int i = l, j = c - su[i];
     int b, t;
     tile_at(nd + i, b, t);
     const int ns = rs[i], np = rk[i];
-    for (int j = 0; j < np; ++j) {
-      const int c = su[i] + j;
-      const int s0 = (int)((int64_t)j * ns / np), s1 = (int)((int64_t)(j + 1) * ns / np);
-      put(c * R + min(c, n_pieces) + R, b, t, s0, s1, np, np > 1 ? sbase[i] + j : -1,
-          np > 1 ? sbase[i] : -1);
-    }
+    const int s0 = j * ns / np, s1 = (j + 1) * ns / np;  // ns < 2^20, np <= kMaxPieces
+    put(c * R + min(c, n_pieces) + R, b, t, s0, s1, np, np > 1 ? sbase[i] + j : -1,
+        np > 1 ? sbase[i] : -1);
   }
 }
 

@@ -1063,10 +1063,17 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
 // its keys through L2); with the causal mask a tile's keys end at its last row, so tiles go
 // from the last tile index down, sequences ranked within each.
 //   - Automatic: the first R = floor(tiles / clusters) rounds deal whole tiles, one per
-//     cluster per round, in snake order (rounds alternate direction).  The fewer than
-//     `clusters` tiles left over are cut into pieces of about equal length, at most one
-//     piece per cluster: the piece length T is the smallest for which they fit, at least
-//     kMinPiece steps, and no tile is cut into more than kMaxPieces pieces.
+//     cluster per round, in list order, alternating direction.  With the tree mask and at
+//     most kMaxRanked sequences (a list sorted longest first) the last kDealtRounds rounds
+//     instead deal their tiles to the clusters in increasing order of the key steps they
+//     already hold (ties by cluster index: the longest-processing-time rule, round by round
+//     so that the tiles of one round still run side by side; the last three rounds dealt
+//     this way even the loads about as well as all of them).  With the causal mask a
+//     round's tiles differ by a step at most.  The fewer than `clusters` tiles left over
+//     are cut into pieces of about equal length, at most one piece per cluster: the piece
+//     length T is the smallest for which they fit, at least kMinPiece steps, and no tile is
+//     cut into more than kMaxPieces pieces.  The pieces, in tile order, go to the clusters
+//     that hold the fewest steps (dealt lists) or to the clusters in index order.
 //   - Forced (num_splits = S): every tile in S pieces of equal step counts, the items in
 //     tile order dealt to the clusters in equal contiguous runs.
 // Each cluster's items are stored consecutively (cl_start[c] .. cl_start[c+1]-1;
@@ -1075,7 +1082,8 @@ gather_kv_kernel(const uint4* __restrict__ ckv, int64_t ckv_stride16, const uint
 constexpr int kMinPiece = 4;
 constexpr int kMaxPieces = 8;
 constexpr int kMaxRanked = 1024;
-constexpr int kMaxSchedClusters = 1024;
+constexpr int kMaxSchedClusters = 256;
+constexpr int kDealtRounds = 3;  // whole-tile rounds dealt by load (the last ones)
 constexpr int kMaxForcedSplits = 32;
 // prep_kernel: threads per block (all of them compute the schedule in block 0), threads
 // that write tensor maps in the other blocks, and the shared buffer (block 0: the
@@ -1083,8 +1091,13 @@ constexpr int kMaxForcedSplits = 32;
 constexpr int kPrepThreads = 1024;
 constexpr int kMapThreads = 128;
 constexpr int kPrepSmem = kMapThreads * 2 * 128;
-static_assert(3 * kMaxRanked * 4 + 4 * kMaxSchedClusters * 4 <= kPrepSmem,
+static_assert(4 * kMaxRanked * 4 + 8 * kMaxSchedClusters * 4 + kDealtRounds * kMaxSchedClusters <=
+                  kPrepSmem,
               "the schedule's lists must fit the prep kernel's shared buffer");
+static_assert(kMaxSchedClusters <= 256, "a dealt tile's cluster is kept in one byte");
+constexpr int kDealLanes = 4;  // lanes that rank one cluster in a dealt round
+static_assert(kMaxSchedClusters * kDealLanes <= kPrepThreads,
+              "the dealt rounds give every cluster its lanes");
 
 struct SchedArgs {
   const int32_t* prefix_len;
@@ -1110,8 +1123,8 @@ __device__ __forceinline__ int tile_steps(const SchedArgs& a, int P, int t) {
 }
 
 __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
-  // All scratch stays in shared memory (`buf`): fewer tiles remain for the quotas than
-  // there are clusters (<= kMaxSchedClusters).
+  // All scratch stays in shared memory (`buf`): fewer tiles are left over than there are
+  // clusters (<= kMaxSchedClusters), and a dealt whole tile's cluster takes one byte.
   int* order = reinterpret_cast<int*>(buf);
   int* sp = order + kMaxRanked;  // prefix length of every sequence (when B <= kMaxRanked)
   int* sc = sp + kMaxRanked;     // its key steps
@@ -1119,6 +1132,12 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   int* sbase = su + kMaxSchedClusters;
   int* rs = sbase + kMaxSchedClusters;
   int* rk = rs + kMaxSchedClusters;
+  int* load = rk + kMaxSchedClusters;    // key steps a cluster holds
+  int* by_rank = load + kMaxSchedClusters;  // clusters in increasing order of load
+  int* rank_of = by_rank + kMaxSchedClusters;
+  int* off = rank_of + kMaxSchedClusters;  // pieces on the clusters before this one
+  int* ss = off + kMaxSchedClusters;       // key steps of the q-th longest sequence
+  unsigned char* tcl = reinterpret_cast<unsigned char*>(ss + kMaxRanked);
   const int B = a.B, T = a.T, ncl = a.ncl;
   const int n_tiles = B * T;
   const bool ranked = B <= kMaxRanked;
@@ -1132,11 +1151,18 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   for (int i = threadIdx.x; ranked && i < B; i += blockDim.x) {
     const int ci = sc[i];
     int rank = 0;
+#pragma unroll 4
     for (int j = 0; j < B; ++j) {
       const int cj = sc[j];
-      rank += (cj > ci) || (cj == ci && j < i);
+      rank += (cj > ci) | ((cj == ci) & (j < i));
     }
     order[rank] = i;
+    ss[rank] = ci;
+  }
+  for (int c = threadIdx.x; c < a.ncl; c += blockDim.x) {
+    load[c] = 0;
+    by_rank[c] = c;
+    rank_of[c] = c;
   }
   __syncthreads();
   auto seq_of = [&](int q) { return ranked ? order[q] : q; };
@@ -1176,92 +1202,170 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   const int R = n_tiles / ncl;  // rounds of whole tiles
   const int nd = R * ncl;
   const int nr = n_tiles - nd;  // tiles left over (fewer than ncl)
+  // The last kDealtRounds rounds are dealt by load when the list is sorted longest first
+  // (tree mask, ranked sequences); with the causal mask a round's tiles differ by a step at
+  // most and alternating rounds do as well.
+  const bool dealt = !a.causal && ranked;
+  const int r0 = dealt ? max(0, R - kDealtRounds) : R;  // first dealt round
+  // The dealing (threads [0, n_deal)) and the cutting of the leftover tiles (threads
+  // [pb, blockDim)) share nothing: they run side by side when enough warps are left over
+  // for the second, else one after the other.
+  const int n_deal = dealt ? (ncl * kDealLanes + 31) / 32 * 32 : 0;
+  const int pb = dealt && n_deal + 128 <= (int)blockDim.x ? n_deal : 0;
+  if (dealt) {
+    // kDealLanes lanes own each cluster (cluster q: threads kDealLanes*q and on) and keep its
+    // load and rank in registers; the loads are shared through two arrays in turn, one read
+    // while the other is written, and the warps that own clusters meet at a named barrier
+    // once a dealt round.  With the tree mask every tile of a sequence sweeps the same
+    // steps: list position pos sweeps ss[pos / T].  The ranking, by (load, index), is
+    // redone only when the order may have changed since it was last taken (a round of equal
+    // tiles adds the same to every load; in the sorted list equal first and last tiles make
+    // such a round).
+    const int q = (int)threadIdx.x / kDealLanes, sub = (int)threadIdx.x % kDealLanes;
+    if ((int)threadIdx.x < n_deal) {
+      // the key steps of the alternating rounds before r0, summed over the owner's lanes
+      int my_load = 0;
+      if (q < ncl)
+        for (int r = sub; r < r0; r += kDealLanes)
+          my_load += ss[(r * ncl + ((r & 1) ? ncl - 1 - q : q)) / T];
+#pragma unroll
+      for (int o = kDealLanes / 2; o > 0; o >>= 1)
+        my_load += __shfl_xor_sync(0xffffffffu, my_load, o);
+      int my_rank = q;
+      int* cur = load;
+      int* nxt = off;  // off is computed later
+      if (q < ncl && sub == 0) cur[q] = my_load;
+      named_sync(1, (uint32_t)n_deal);
+      auto rank_own = [&]() {
+        int n = 0;
+        if (q < ncl) {
+#pragma unroll 4
+          for (int j = sub; j < ncl; j += kDealLanes) {
+            const int lj = cur[j];
+            n += (lj < my_load) | ((lj == my_load) & (j < q));
+          }
+        }
+#pragma unroll
+        for (int o = kDealLanes / 2; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+        my_rank = n;
+      };
+      bool stale = r0 > 0;
+      for (int r = r0; r < R; ++r) {
+        const int first = ss[(r * ncl) / T];
+        const int last = ss[(r * ncl + ncl - 1) / T];
+        if (stale) rank_own();
+        if (q < ncl) {
+          const int pos = r * ncl + my_rank;
+          my_load += ss[pos / T];
+          if (sub == 0) {
+            nxt[q] = my_load;
+            tcl[(r - r0) * ncl + my_rank] = (unsigned char)q;
+          }
+        }
+        named_sync(1, (uint32_t)n_deal);
+        int* tmp = cur;
+        cur = nxt;
+        nxt = tmp;
+        stale = first != last;
+      }
+      if (stale && nr > 0) rank_own();
+      if (q < ncl && sub == 0) {
+        by_rank[my_rank] = q;
+        rank_of[q] = my_rank;
+      }
+    }
+    if (pb == 0) __syncthreads();
+  }
   // The leftover tiles are cut into equal pieces, at most one per cluster: tile i into
   // k_i = ceil(ns_i / T) pieces (an empty tile: one), with T the smallest piece length for
   // which the pieces fit the clusters.  T is at least kMinPiece steps and cuts no tile into
-  // more than kMaxPieces pieces.  Every warp tests one candidate length per round (the
-  // piece count falls as the length grows), so two or three rounds find T; warp 0 then
-  // takes the prefix sums (fewer than ncl leftover tiles).
+  // more than kMaxPieces pieces.  Every warp of the group tests one candidate length per
+  // round (the piece count falls as the length grows), so two or three rounds find T; the
+  // group's first warp then takes the prefix sums (fewer than ncl leftover tiles).
   __shared__ int s_pieces, s_slots, s_mx, s_lo, s_hi;
   __shared__ int s_fit[32];
-  if (threadIdx.x == 0) s_mx = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-    int b, t;
-    tile_at(nd + i, b, t);
-    rs[i] = tile_steps(a, P_of(b), t);
-    atomicMax(&s_mx, rs[i]);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int mx = s_mx;
-    s_lo = max(kMinPiece, (mx + kMaxPieces - 1) / kMaxPieces);
-    s_hi = max(s_lo, mx);  // count(hi) <= nr < ncl: hi fits
-  }
-  __syncthreads();
-  {
-    const int nw = min((int)(blockDim.x >> 5), 32), w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (;;) {
-      const int lo = s_lo, hi = s_hi;
-      if (lo >= hi) break;
-      const int stride = (hi - lo + nw - 1) / nw;
-      const int len = lo + w * stride;
-      if (w < nw && len < hi) {
-        int c = 0;
-        for (int i = lane; i < nr; i += 32) c += max(1, (rs[i] + len - 1) / len);
+  const int pt = (int)threadIdx.x - pb, npt = (int)blockDim.x - pb;  // multiples of 32
+  if (pt >= 0) {
+    if (pt == 0) s_mx = 0;
+    named_sync(2, (uint32_t)npt);
+    for (int i = pt; i < nr; i += npt) {
+      int b, t;
+      tile_at(nd + i, b, t);
+      rs[i] = tile_steps(a, P_of(b), t);
+      atomicMax(&s_mx, rs[i]);
+    }
+    named_sync(2, (uint32_t)npt);
+    if (pt == 0) {
+      const int mx = s_mx;
+      s_lo = max(kMinPiece, (mx + kMaxPieces - 1) / kMaxPieces);
+      s_hi = max(s_lo, mx);  // count(hi) <= nr < ncl: hi fits
+    }
+    named_sync(2, (uint32_t)npt);
+    {
+      const int nw = min(npt >> 5, 32), w = pt >> 5, lane = pt & 31;
+      for (;;) {
+        const int lo = s_lo, hi = s_hi;
+        if (lo >= hi) break;
+        const int stride = (hi - lo + nw - 1) / nw;
+        const int len = lo + w * stride;
+        if (w < nw && len < hi) {
+          int c = 0;
+          for (int i = lane; i < nr; i += 32) c += max(1, (rs[i] + len - 1) / len);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        if (lane == 0) s_fit[w] = c <= ncl ? 1 : 0;
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        // candidates in increasing length: the first that fits is the new upper end, the
-        // one before it (which does not) sets the new lower end
-        int nlo = lo, nhi = hi;
-        for (int ww = 0; ww < nw; ++ww) {
-          const int l2 = lo + ww * stride;
-          if (l2 >= hi) break;
-          if (s_fit[ww]) {
-            nhi = l2;
-            break;
+          for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+          if (lane == 0) s_fit[w] = c <= ncl ? 1 : 0;
+        }
+        named_sync(2, (uint32_t)npt);
+        if (pt < 32) {
+          // candidates in increasing length: the first that fits is the new upper end, the
+          // one before it (which does not) sets the new lower end
+          const int l2 = lo + pt * stride;
+          const uint32_t fit = __ballot_sync(0xffffffffu, pt < nw && l2 < hi && s_fit[pt]);
+          if (pt == 0) {
+            const int f = fit ? __ffs(fit) - 1 : -1;  // first candidate that fits
+            const int tested = min(nw, (hi - lo + stride - 1) / stride);
+            if (f >= 0) {
+              s_lo = f > 0 ? lo + (f - 1) * stride + 1 : lo;
+              s_hi = lo + f * stride;
+            } else {
+              s_lo = lo + (tested - 1) * stride + 1;
+            }
           }
-          nlo = l2 + 1;
         }
-        s_lo = nlo;
-        s_hi = nhi;
+        named_sync(2, (uint32_t)npt);
       }
-      __syncthreads();
     }
-  }
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int lo = s_lo;
-    // k_i, first piece su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time)
-    int run_c = 0, run_s = 0;
-    for (int i0 = 0; i0 < nr; i0 += 32) {
-      const int i = i0 + lane;
-      const int k = i < nr ? max(1, (rs[i] + lo - 1) / lo) : 0;
-      const int ks = k > 1 ? k : 0;
-      int ic = k, is = ks;
+    if (pt < 32) {
+      const int lane = pt;
+      const int lo = s_lo;
+      // k_i, first piece su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time)
+      int run_c = 0, run_s = 0;
+      for (int i0 = 0; i0 < nr; i0 += 32) {
+        const int i = i0 + lane;
+        const int k = i < nr ? max(1, (rs[i] + lo - 1) / lo) : 0;
+        const int ks = k > 1 ? k : 0;
+        int ic = k, is = ks;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int vc = __shfl_up_sync(0xffffffffu, ic, o), vs = __shfl_up_sync(0xffffffffu, is, o);
-        if (lane >= o) {
-          ic += vc;
-          is += vs;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+          const int vs = __shfl_up_sync(0xffffffffu, is, o);
+          if (lane >= o) {
+            ic += vc;
+            is += vs;
+          }
         }
+        if (i < nr) {
+          su[i] = run_c + ic - k;
+          sbase[i] = run_s + is - ks;
+          rk[i] = k;
+        }
+        run_c += __shfl_sync(0xffffffffu, ic, 31);
+        run_s += __shfl_sync(0xffffffffu, is, 31);
       }
-      if (i < nr) {
-        su[i] = run_c + ic - k;
-        sbase[i] = run_s + is - ks;
-        rk[i] = k;
+      if (lane == 0) {
+        s_pieces = run_c;
+        s_slots = run_s;
       }
-      run_c += __shfl_sync(0xffffffffu, ic, 31);
-      run_s += __shfl_sync(0xffffffffu, is, 31);
-    }
-    if (lane == 0) {
-      s_pieces = run_c;
-      s_slots = run_s;
     }
   }
   __syncthreads();
@@ -1274,8 +1378,19 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
     for (int c = threadIdx.x; c <= ncl; c += blockDim.x) a.cl_start[c] = 0;
     return;
   }
-  // cluster c: its R whole tiles, then one piece if c < n_pieces
-  for (int c = threadIdx.x; c < ncl; c += blockDim.x) a.cl_start[c] = c * R + min(c, n_pieces);
+  // piece k goes to cluster by_rank[k]; off[c] counts the pieces on clusters before c
+  if (threadIdx.x < 32) {
+    int run = 0;
+    for (int c0 = 0; c0 < ncl; c0 += 32) {
+      const int c = c0 + (int)threadIdx.x;
+      const uint32_t m = __ballot_sync(0xffffffffu, c < ncl && rank_of[c] < n_pieces);
+      if (c < ncl) off[c] = run + __popc(m & ((1u << threadIdx.x) - 1u));
+      run += __popc(m);
+    }
+  }
+  __syncthreads();
+  // cluster c: its R whole tiles, then one piece if it was given one
+  for (int c = threadIdx.x; c < ncl; c += blockDim.x) a.cl_start[c] = c * R + off[c];
   if (threadIdx.x == 0) {
     a.cl_start[ncl] = nd + n_pieces;
     a.cl_start[ncl + 1] = n_slots;
@@ -1283,25 +1398,25 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   // whole tiles of the first R rounds
   for (int pos = threadIdx.x; pos < nd; pos += blockDim.x) {
     const int r = pos / ncl, i = pos - r * ncl;
-    const int c = (r & 1) ? ncl - 1 - i : i;
+    const int c = r >= r0 ? (int)tcl[pos - r0 * ncl] : ((r & 1) ? ncl - 1 - i : i);
     int b, t;
     tile_at(pos, b, t);
-    put(c * R + min(c, n_pieces) + r, b, t, 0, tile_steps(a, P_of(b), t), 1, -1, -1);
+    put(c * R + off[c] + r, b, t, 0, tile_steps(a, P_of(b), t), 1, -1, -1);
   }
-  // the pieces of the leftover tiles, one thread per piece: piece c (cluster c) belongs
-  // to the last tile i with su[i] <= c
-  for (int c = threadIdx.x; c < n_pieces; c += blockDim.x) {
+  // the pieces of the leftover tiles, one thread per piece: piece k belongs to the last
+  // tile i with su[i] <= k
+  for (int k = (int)blockDim.x - 1 - (int)threadIdx.x; k < n_pieces; k += blockDim.x) {
     int l = 0, h = nr - 1;
     while (l < h) {
       const int m = (l + h + 1) >> 1;
-      if (su[m] <= c) l = m; else h = m - 1;
+      if (su[m] <= k) l = m; else h = m - 1;
     }
-    const int i = l, j = c - su[i];
+    const int i = l, j = k - su[i], c = by_rank[k];
     int b, t;
     tile_at(nd + i, b, t);
     const int ns = rs[i], np = rk[i];
     const int s0 = j * ns / np, s1 = (j + 1) * ns / np;  // ns < 2^20, np <= kMaxPieces
-    put(c * R + min(c, n_pieces) + R, b, t, s0, s1, np, np > 1 ? sbase[i] + j : -1,
+    put(c * R + off[c] + R, b, t, s0, s1, np, np > 1 ? sbase[i] + j : -1,
         np > 1 ? sbase[i] : -1);
   }
 }
@@ -1614,8 +1729,7 @@ TcPlan tc_plan(const tv_attn_args* a) {
     p.n_items = p.n_tiles * p.splits;
     p.max_slots = p.splits > 1 ? p.n_items : 0;
   } else {
-    // whole tiles, plus at most one piece more per cluster from the quotas; at most two
-    // pieces of split tiles per cluster (its first and its last)
+    // whole tiles, plus at most one piece per cluster (slots: twice that, a loose bound)
     p.n_items = p.n_tiles + p.clusters;
     p.max_slots = 2 * (int64_t)p.clusters;
   }
@@ -1751,8 +1865,8 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     p.test_exit_counts = g_test_exit_counts;
   }
   if (pl.n_tiles == 0) return cudaSuccess;
-  // clusters launched: all of them (the quotas spread the work), or with forced splits no
-  // more than there are items
+  // clusters launched: all of them (the schedule spreads the work over all), or with
+  // forced splits no more than there are items
   const int ncl = (int)std::min<int64_t>(pl.clusters, pl.splits > 0 ? pl.n_items : pl.clusters);
 
   {

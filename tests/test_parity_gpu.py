@@ -425,3 +425,16 @@ def test_rope_bf16_store_equals_rounded_float32_result(in_dt):
     tv.rope_neox(x, o16, Pt, dt)
     torch.cuda.synchronize()
     assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("B,lo,hi", [(2, 1500, 3000), (9, 2000, 2600), (76, 1, 600),
+                                      (80, 1, 300)])
+def test_schedule_shapes_tensor_cores(B, lo, hi):
+    """Batch sizes whose row tiles (17 per sequence at q_len 33, 64 heads) fall below, just
+    past, exactly on and past a whole number of rounds over the 76 clusters of a GB300: every
+    tile split in pieces; two rounds and one tile split; whole rounds only; 68 tiles left
+    over, one piece each.  Ragged prefixes in a paged cache, every sequence against the
+    oracle."""
+    inp = synth.generate("cfg5_bf16", B=B, prefix=(lo, hi), seed=500 + B)
+    step, g, o = run_pair(inp, path=tv.PATH_TCGEN05)
+    check_step(inp, g, o)

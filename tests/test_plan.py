@@ -90,8 +90,8 @@ def test_workspace_holds_what_the_plan_keeps_there(tvlib):
     rows = 32 * 33 * 64
     tiles = 32 * 17
     base = workspace(args(32, 64, 33, 8192))
-    # automatic schedule: item records plus partial results for the split pieces of the
-    # equal quotas (at most two per cluster, 74 clusters assumed without a GPU)
+    # automatic schedule: item records plus partial results for the pieces of split tiles
+    # (room for two per cluster, 74 clusters assumed without a GPU)
     assert base >= 2 * 74 * 128 * (512 + 1) * 4
     assert base < 64 << 20
     ws2 = workspace(args(32, 64, 33, 8192, num_splits=2))

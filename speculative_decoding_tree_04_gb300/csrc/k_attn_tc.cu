@@ -45,9 +45,10 @@
 // workspace instead.
 //
 // The schedule (computed by prep_kernel on the device from the prefix lengths): whole
-// 128-row tiles are dealt to the persistent clusters longest first in snake rounds; the
-// tiles left over are cut into pieces of about equal length, one piece per cluster.  The
-// pieces of a split tile write partial results that merge_kernel combines.
+// 128-row tiles are dealt to the persistent clusters longest first in rounds, the last
+// rounds to the least-loaded clusters; the tiles left over are cut into pieces of about
+// equal length, at most one piece per cluster.  The pieces of a split tile write partial
+// results that merge_kernel combines.
 //
 // Every wait is bounded (a wall-clock deadline); on expiry the kernel records
 // TV_ERR_TIMEOUT, tells the peer CTA, drains its tensor-core work, frees its TMEM and

@@ -8,6 +8,9 @@ queries, the latent KV cache, outputs) and runs, on one CUDA stream:
     tv_rope_neox(kpe_tree -> cache rows P + i)      -> rotated draft-token k_pe in cache
     tv_verify_attn(...)                             -> out [B,Q,H,DL], lse [B,Q,H]
 
+``HostStepPipeline`` runs steps whose inputs and results live in host memory, with each
+step's copies overlapping its neighbours' work.
+
 This module moves bytes and issues calls; all arithmetic runs in libtv's kernels.
 """
 from __future__ import annotations
@@ -179,3 +182,69 @@ class VerifyStep:
                     k_pe_cache=self.k_pe.float().cpu().numpy(),
                     out=self.out.cpu().numpy(), lse=self.lse.cpu().numpy(),
                     status=int(self.status.item()))
+
+
+class HostStepPipeline:
+    """Verify steps whose inputs and results live in host memory, pipelined on the GPU.
+
+    Two device buffer sets (two ``VerifyStep``) and three CUDA streams: step i uploads its
+    inputs (pinned host tensors, keyed like ``VerifyStep.HOST_KEYS``) into buffer set i % 2
+    on the upload stream, runs on the compute stream once its upload is done, and
+    downloads out and lse into the host tensors given for it on the download stream once
+    it has run.  So step i + 1's upload overlaps step i's compute and step i's download,
+    and a buffer set is reused only after its previous download has finished.  Every step
+    still copies all of its inputs in and its results out.  ``synchronize()`` waits for all
+    submitted steps; results must not be read before it."""
+
+    def __init__(self, inp: dict, device="cuda", **step_kw):
+        self.device = torch.device(device)
+        self.steps = [VerifyStep(inp, device=self.device, **step_kw) for _ in range(2)]
+        self.streams = [torch.cuda.Stream(self.device) for _ in range(3)]
+        self._done = [None, None]
+        self._n = 0
+
+    def _dst(self, st: "VerifyStep") -> dict:
+        return {"q_latent": st.q_latent, "q_pe": st.q_pe_raw, "kpe_tree": st.kpe_tree,
+                "ckv_tree": st.ckv_tree, "c_kv": st.c_kv, "k_pe": st.k_pe,
+                "parent": st.parent, "prefix_len": st.prefix_len, "page_table": st.page_table}
+
+    def submit(self, host_in: dict, out_h: torch.Tensor, lse_h: torch.Tensor):
+        """Queue one step: copy ``host_in`` (name -> pinned tensor) in, run, copy out and
+        lse into the pinned ``out_h`` and ``lse_h``.  Returns at once."""
+        b = self._n % 2
+        self._n += 1
+        st = self.steps[b]
+        dst = self._dst(st)
+        s_in, s_c, s_out = self.streams
+        start = torch.cuda.Event()
+        start.record(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(start)
+            if self._done[b] is not None:
+                s_in.wait_event(self._done[b])
+            for k, t in host_in.items():
+                dst[k].copy_(t, non_blocking=True)
+            e_in = torch.cuda.Event()
+            e_in.record(s_in)
+        with torch.cuda.stream(s_c):
+            s_c.wait_event(e_in)
+            st.run(s_c)
+            e_c = torch.cuda.Event()
+            e_c.record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e_c)
+            out_h.copy_(st.out, non_blocking=True)
+            lse_h.copy_(st.lse, non_blocking=True)
+            e_o = torch.cuda.Event()
+            e_o.record(s_out)
+            self._done[b] = e_o
+
+    def wait_on(self, stream=None):
+        """Make ``stream`` (default: the current one) wait for every submitted step."""
+        cur = stream if stream is not None else torch.cuda.current_stream(self.device)
+        for s in self.streams:
+            cur.wait_stream(s)
+
+    def synchronize(self):
+        for s in self.streams:
+            s.synchronize()

@@ -130,3 +130,44 @@ def test_overlapped_step_parity_all_forms(name, kw, form):
     step.c_kv[rows] = 0                       # the prologue's append must restore these
     step.run()
     check_step(inp, step.results(), oracle.tree_verify_step(inp))
+
+
+@pytest.mark.parametrize("name,kw", [("cfg4_bf16", {}), ("cfg3_bf16", {}), ("cfg1_fp32", {})])
+def test_host_pipeline_equals_single_steps(name, kw):
+    """Steps with host-resident inputs and results, pipelined over two device buffer sets,
+    give the results of the same steps run one at a time, bit for bit, and every step
+    reads its own inputs (the steps here alternate between two different input sets)."""
+    from speculative_decoding_tree_04_gb300.step import HostStepPipeline, _dev_float
+    base = synth.generate(name, **kw)
+    other = dict(base)  # same sizes, queries negated
+    for k in ("q_latent", "q_pe"):
+        other[k] = -base[k]
+        if base["kv_dtype"] == "bf16":
+            other[k + "_bits"] = base[k + "_bits"] ^ np.uint16(0x8000)
+    inps = [base, other]
+    want = []
+    for inp in inps:
+        st = VerifyStep(inp, fused=True)
+        st.run()
+        r = st.results()
+        want.append((r["out"], r["lse"]))
+    pipe = HostStepPipeline(inps[0], fused=True)
+    hosts = []
+    for inp in inps:
+        h = {k: _dev_float(inp, k, "cuda", pin=True)
+             for k in ("q_latent", "q_pe", "kpe_tree", "ckv_tree", "c_kv", "k_pe")}
+        h["parent"] = torch.from_numpy(inp["parent"]).pin_memory()
+        h["prefix_len"] = torch.from_numpy(inp["prefix_len"]).pin_memory()
+        if inp["page_table"] is not None:
+            h["page_table"] = torch.from_numpy(inp["page_table"]).pin_memory()
+        hosts.append(h)
+    shape_o, shape_l = want[0][0].shape, want[0][1].shape
+    outs = [(torch.empty(shape_o, dtype=torch.float32).pin_memory(),
+             torch.empty(shape_l, dtype=torch.float32).pin_memory()) for _ in range(6)]
+    for i in range(6):
+        pipe.submit(hosts[i % 2], *outs[i])
+    pipe.synchronize()
+    for i in range(6):
+        o, l = want[i % 2]
+        assert np.array_equal(outs[i][0].numpy(), o)
+        assert np.array_equal(outs[i][1].numpy(), l)

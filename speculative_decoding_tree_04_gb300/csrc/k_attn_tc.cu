@@ -1108,6 +1108,7 @@ struct SchedArgs {
   int4* items;
   int32_t* cl_start;
   int4* slot_info;
+  int4* split_info;  // the merge's work list: per split tile {b, t, pieces, first slot}
   int32_t* status;
 };
 
@@ -1193,10 +1194,14 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
       const int ns = tile_steps(a, P_of(b), t);
       put(k, b, t, (int)((int64_t)j * ns / S), (int)((int64_t)(j + 1) * ns / S), S,
           S > 1 ? k : -1, S > 1 ? pos * S : -1);
+      if (S > 1 && j == 0) a.split_info[pos] = make_int4(b, t, S, pos * S);
     }
     for (int c = threadIdx.x; c <= ncl; c += blockDim.x)
       a.cl_start[c] = (int)(((int64_t)c * n_items + ncl - 1) / ncl);
-    if (threadIdx.x == 0) a.cl_start[ncl + 1] = S > 1 ? n_items : 0;
+    if (threadIdx.x == 0) {
+      a.cl_start[ncl + 1] = S > 1 ? n_items : 0;
+      a.cl_start[ncl + 2] = S > 1 ? n_tiles : 0;
+    }
     return;
   }
 
@@ -1283,7 +1288,7 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   // more than kMaxPieces pieces.  Every warp of the group tests one candidate length per
   // round (the piece count falls as the length grows), so two or three rounds find T; the
   // group's first warp then takes the prefix sums (fewer than ncl leftover tiles).
-  __shared__ int s_pieces, s_slots, s_mx, s_lo, s_hi;
+  __shared__ int s_pieces, s_slots, s_split, s_mx, s_lo, s_hi;
   __shared__ int s_fit[32];
   const int pt = (int)threadIdx.x - pb, npt = (int)blockDim.x - pb;  // multiples of 32
   if (pt >= 0) {
@@ -1339,8 +1344,9 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
     if (pt < 32) {
       const int lane = pt;
       const int lo = s_lo;
-      // k_i, first piece su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time)
-      int run_c = 0, run_s = 0;
+      // k_i, first piece su[i] and first slot sbase[i] (exclusive prefix sums, 32 at a time);
+      // the split tiles (k_i > 1) listed in order for the merge
+      int run_c = 0, run_s = 0, run_q = 0;
       for (int i0 = 0; i0 < nr; i0 += 32) {
         const int i = i0 + lane;
         const int k = i < nr ? max(1, (rs[i] + lo - 1) / lo) : 0;
@@ -1355,17 +1361,26 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
             is += vs;
           }
         }
+        const uint32_t split = __ballot_sync(0xffffffffu, k > 1);
         if (i < nr) {
           su[i] = run_c + ic - k;
           sbase[i] = run_s + is - ks;
           rk[i] = k;
+          if (k > 1) {
+            int b, t;
+            tile_at(nd + i, b, t);
+            a.split_info[run_q + __popc(split & ((1u << lane) - 1u))] =
+                make_int4(b, t, k, run_s + is - ks);
+          }
         }
         run_c += __shfl_sync(0xffffffffu, ic, 31);
         run_s += __shfl_sync(0xffffffffu, is, 31);
+        run_q += __popc(split);
       }
       if (lane == 0) {
         s_pieces = run_c;
         s_slots = run_s;
+        s_split = run_q;
       }
     }
   }
@@ -1375,6 +1390,7 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
     if (threadIdx.x == 0) {
       report(a.status, TV_ERR_UNSUPPORTED);
       a.cl_start[ncl + 1] = 0;
+      a.cl_start[ncl + 2] = 0;
     }
     for (int c = threadIdx.x; c <= ncl; c += blockDim.x) a.cl_start[c] = 0;
     return;
@@ -1395,6 +1411,7 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   if (threadIdx.x == 0) {
     a.cl_start[ncl] = nd + n_pieces;
     a.cl_start[ncl + 1] = n_slots;
+    a.cl_start[ncl + 2] = s_split;
   }
   // whole tiles of the first R rounds
   for (int pos = threadIdx.x; pos < nd; pos += blockDim.x) {
@@ -1422,72 +1439,74 @@ __device__ void schedule(const SchedArgs& a, unsigned char* buf) {
   }
 }
 
-// Merge of split tiles, after the attention kernel: one warp per row of a tile whose
-// first slot is blockIdx.x (8 rows per block).  Lane k < pieces takes piece k's
+// Merge of split tiles, after the attention kernel: one warp per row, 8 rows per work unit,
+// 16 units per split tile, the units dealt to the blocks in turn (a grid of one wave, so
+// that no block is launched only to find no work).  Lane k < pieces takes piece k's
 // log-sum-exp; then, in slot order,
 //   lse = ln sum_k exp(lse_k),  out = sum_k exp(lse_k - lse) out_k
 // with four 16-byte columns per lane in flight.
-__global__ void __launch_bounds__(256)
-merge_kernel(const int4* __restrict__ slot_info, const int32_t* __restrict__ n_slots,
+__global__ void __launch_bounds__(256, 2)
+merge_kernel(const int4* __restrict__ split_info, const int32_t* __restrict__ n_split,
              const float* __restrict__ ws_out, const float* __restrict__ ws_lse, int rows_seq,
              float* __restrict__ out, float* __restrict__ lse) {
-  const int s = blockIdx.x;
-  if (s >= __ldg(n_slots)) return;
-  const int4 si = __ldg(slot_info + s);  // {b, t, pieces, first slot}
-  if (si.w != s) return;                 // not the first slot of its tile
+  const int units = __ldg(n_split) * (kRows / 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.y * 8 + warp;
-  const int trow = si.y * kRows + row;
-  if (trow >= rows_seq) return;
-  const int64_t grow = (int64_t)si.x * rows_seq + trow;
-  const int np = si.z;
-  const float ls = lane < np ? ws_lse[(int64_t)(s + lane) * kRows + row] : -INFINITY;
-  float mx = ls;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int4 si = __ldg(split_info + u / (kRows / 8));  // {b, t, pieces, first slot}
+    const int s = si.w;
+    const int row = (u % (kRows / 8)) * 8 + warp;
+    const int trow = si.y * kRows + row;
+    if (trow >= rows_seq) continue;
+    const int64_t grow = (int64_t)si.x * rows_seq + trow;
+    const int np = si.z;
+    const float ls = lane < np ? ws_lse[(int64_t)(s + lane) * kRows + row] : -INFINITY;
+    float mx = ls;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const float e = (lane < np && mx != -INFINITY && ls != -INFINITY) ? expf(ls - mx) : 0.f;
-  float wsum = 0.f;
-  for (int k = 0; k < np; ++k) wsum += __shfl_sync(0xffffffffu, e, k);
-  const float w = wsum > 0.f ? e / wsum : 0.f;
-  float4 acc[4];
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float e = (lane < np && mx != -INFINITY && ls != -INFINITY) ? expf(ls - mx) : 0.f;
+    float wsum = 0.f;
+    for (int k = 0; k < np; ++k) wsum += __shfl_sync(0xffffffffu, e, k);
+    const float w = wsum > 0.f ? e / wsum : 0.f;
+    float4 acc[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // four pieces' loads in flight at a time (a piece at a time left the warp waiting on
-  // one memory round trip per piece); the products are summed in piece order as before
-  for (int k0 = 0; k0 < np; k0 += 4) {
-    float wk[4];
-    float4 v[4][4];
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // four pieces' loads in flight at a time (a piece at a time left the warp waiting on
+    // one memory round trip per piece); the products are summed in piece order as before
+    for (int k0 = 0; k0 < np; k0 += 4) {
+      float wk[4];
+      float4 v[4][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = k0 + q;
-      wk[q] = __shfl_sync(0xffffffffu, w, k < np ? k : 0);
-      if (k >= np) wk[q] = 0.f;
-      if (wk[q] != 0.f) {  // the same for the whole warp
-        const float4* src =
-            reinterpret_cast<const float4*>(ws_out + ((int64_t)(s + k) * kRows + row) * kDL);
+      for (int q = 0; q < 4; ++q) {
+        const int k = k0 + q;
+        wk[q] = __shfl_sync(0xffffffffu, w, k < np ? k : 0);
+        if (k >= np) wk[q] = 0.f;
+        if (wk[q] != 0.f) {  // the same for the whole warp
+          const float4* src =
+              reinterpret_cast<const float4*>(ws_out + ((int64_t)(s + k) * kRows + row) * kDL);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[q][i] = __ldcs(src + lane + 32 * i);
-      } else {
+          for (int i = 0; i < 4; ++i) v[q][i] = __ldcs(src + lane + 32 * i);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[q][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int i = 0; i < 4; ++i) v[q][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (wk[q] == 0.f) continue;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i].x = fmaf(wk[q], v[q][i].x, acc[i].x);
+          acc[i].y = fmaf(wk[q], v[q][i].y, acc[i].y);
+          acc[i].z = fmaf(wk[q], v[q][i].z, acc[i].z);
+          acc[i].w = fmaf(wk[q], v[q][i].w, acc[i].w);
+        }
       }
     }
+    float4* d4 = reinterpret_cast<float4*>(out + grow * kDL);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (wk[q] == 0.f) continue;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i].x = fmaf(wk[q], v[q][i].x, acc[i].x);
-        acc[i].y = fmaf(wk[q], v[q][i].y, acc[i].y);
-        acc[i].z = fmaf(wk[q], v[q][i].z, acc[i].z);
-        acc[i].w = fmaf(wk[q], v[q][i].w, acc[i].w);
-      }
-    }
+    for (int i = 0; i < 4; ++i) d4[lane + 32 * i] = acc[i];
+    if (lane == 0) lse[grow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
   }
-  float4* d4 = reinterpret_cast<float4*>(out + grow * kDL);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d4[lane + 32 * i] = acc[i];
-  if (lane == 0) lse[grow] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
 // Work preparation, one launch before the attention kernel.
@@ -1729,19 +1748,22 @@ TcPlan tc_plan(const tv_attn_args* a) {
   if (p.splits > 0) {
     p.n_items = p.n_tiles * p.splits;
     p.max_slots = p.splits > 1 ? p.n_items : 0;
+    p.max_split = p.splits > 1 ? p.n_tiles : 0;
   } else {
     // whole tiles, plus at most one piece per cluster (slots: twice that, a loose bound)
     p.n_items = p.n_tiles + p.clusters;
     p.max_slots = 2 * (int64_t)p.clusters;
+    p.max_split = p.clusters;  // split tiles are among the fewer than `clusters` left over
   }
   return p;
 }
 
-// Workspace: [item records: 32 B each][cluster list starts][slot records][partial
-// outputs: slot x 128 x 512 fp32][partial lse][paged
+// Workspace: [item records: 32 B each][cluster list starts, then the item, slot and
+// split-tile counts][slot records][split-tile records][partial outputs: slot x 128 x 512
+// fp32][partial lse][paged
 // cache: gathered key view, or per-step tensor maps (2 x 128 B per step) and swap flags].
 struct TcWs {
-  size_t items, cl_start, slot_info, part_out, part_lse, tail, total;
+  size_t items, cl_start, slot_info, split_info, part_out, part_lse, tail, total;
 };
 TcWs tc_ws_layout(const tv_attn_args* a, const TcPlan& p) {
   TcWs w{};
@@ -1749,9 +1771,11 @@ TcWs tc_ws_layout(const tv_attn_args* a, const TcPlan& p) {
   w.items = n;
   n += align256((size_t)p.n_items * 32);
   w.cl_start = n;
-  n += align256(((size_t)p.clusters + 2) * 4);
+  n += align256(((size_t)p.clusters + 3) * 4);
   w.slot_info = n;
   n += align256((size_t)p.max_slots * 16);
+  w.split_info = n;
+  n += align256((size_t)p.max_split * 16);
   w.part_out = n;
   n += align256((size_t)p.max_slots * kRows * kDL * 4);
   w.part_lse = n;
@@ -1886,6 +1910,7 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
     sa.items = (int4*)(ws0 + lay.items);
     sa.cl_start = (int32_t*)(ws0 + lay.cl_start);
     sa.slot_info = (int4*)(ws0 + lay.slot_info);
+    sa.split_info = (int4*)(ws0 + lay.split_info);
     sa.status = a->status;
     const int64_t map_blocks = paged ? (a->B * steps + kMapThreads - 1) / kMapThreads : 0;
     cudaLaunchConfig_t pc = {};
@@ -1930,9 +1955,12 @@ cudaError_t launch_attn_tc(const tv_attn_args* a, const TcPlan& pl, void* ws, cu
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, m_lat_s, m_kpe_s, m_lat_o, m_q, m_qr);
   if (e != cudaSuccess || pl.max_slots == 0) return e;
-  // merge the pieces of split tiles (blocks of unused slots leave at once)
-  merge_kernel<<<dim3((unsigned)pl.max_slots, kRows / 8), 256, 0, st>>>(
-      (const int4*)(ws0 + lay.slot_info), (const int32_t*)(ws0 + lay.cl_start) + ncl + 1,
+  // merge the pieces of split tiles: two blocks per SM (one wave at the merge's register
+  // count), or fewer when there cannot be that many units of work
+  const int64_t merge_blocks =
+      std::min<int64_t>(pl.max_split * (kRows / 8), 4 * (int64_t)pl.clusters);
+  merge_kernel<<<(unsigned)merge_blocks, 256, 0, st>>>(
+      (const int4*)(ws0 + lay.split_info), (const int32_t*)(ws0 + lay.cl_start) + ncl + 2,
       p.ws_out, p.ws_lse, a->Q * a->H, a->out, a->lse);
   return cudaGetLastError();
 }

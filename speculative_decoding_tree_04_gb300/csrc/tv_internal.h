@@ -59,9 +59,10 @@ struct TcPlan {
   int clusters;       // persistent 2-CTA clusters launched (at most)
   int tiles_per_seq;  // ceil(Q*H / 128)
   int64_t n_tiles;    // B * tiles_per_seq
-  int splits;         // 0: whole tiles then equal quotas; S > 0: every tile in S pieces
+  int splits;         // 0: the automatic schedule; S > 0: every tile in S pieces
   int64_t n_items;    // work items at most
   int64_t max_slots;  // partial-result slots of split tiles at most
+  int64_t max_split;  // split tiles at most (records of the merge's work list)
 };
 bool tc_supported(const tv_attn_args* a);
 TcPlan tc_plan(const tv_attn_args* a);

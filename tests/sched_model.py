@@ -16,10 +16,12 @@ this model is written from the rules the kernel source documents:
     the clusters; piece k goes to the k-th least-loaded cluster (sorted lists) or to
     cluster k;
   * each cluster's items lie consecutively, its whole tiles in round order and its piece
-    last; the pieces of a split tile take consecutive partial-result slots.
+    last; the pieces of a split tile take consecutive partial-result slots, and the split
+    tiles are listed in tile order for the merge.
 
 ``schedule`` returns the arrays the preparation kernel writes: the item records, the list
-starts (with the number of items and of slots appended) and the slot records.
+starts (with the numbers of items, of slots and of split tiles appended), the slot records
+and the split-tile records.
 """
 from __future__ import annotations
 
@@ -106,7 +108,8 @@ def schedule(prefix_len, Q, H, causal, max_prefix, seq_cap, ncl):
     for c in range(ncl):
         off.append(run)
         run += has_piece[c]
-    cl_start = [c * R + off[c] for c in range(ncl)] + [nd + n_pieces, n_slots]
+    splits = [(*tile_at(nd + i), k[i], sbase[i]) for i in range(nr) if k[i] > 1]
+    cl_start = [c * R + off[c] for c in range(ncl)] + [nd + n_pieces, n_slots, len(splits)]
 
     items = [None] * (nd + n_pieces)
     slot_info = [None] * n_slots
@@ -127,7 +130,7 @@ def schedule(prefix_len, Q, H, causal, max_prefix, seq_cap, ncl):
         items[c * R + off[c] + R] = (b, t, s0, s1, int(prefix_len[b]), np_, slot, base)
         if slot >= 0:
             slot_info[slot] = (b, t, np_, base)
-    return items, cl_start, slot_info, load
+    return items, cl_start, slot_info, splits
 
 
 def cluster_steps(items, cl_start, ncl):

@@ -1,8 +1,8 @@
 """The tensor-core path's work schedule, read back from the workspace after a call.
 
 The preparation kernel writes, into the call's workspace, the item records (which 128-key
-steps of which 128-row tile each cluster sweeps), each cluster's list start and the records
-of the partial-result slots.  These tests compare them, entry by entry, with the plain
+steps of which 128-row tile each cluster sweeps), each cluster's list start, the records
+of the partial-result slots and the list of split tiles the merge works through.  These tests compare them, entry by entry, with the plain
 Python statement of the rules in ``tests/sched_model.py``, and check independently of it
 that every tile's key steps are swept exactly once.  The attention inputs are zeros: the
 schedule depends only on the sizes and the prefix lengths.
@@ -23,10 +23,12 @@ def align256(n):
 
 def clusters_from_size(total, n_tiles):
     """Clusters the plan used, from the workspace size of a contiguous-cache call (items,
-    list starts, two slots per cluster of records, partial outputs and log-sum-exps)."""
+    list starts and counts, two slots per cluster of records, one split-tile record per
+    cluster, partial outputs and log-sum-exps)."""
     found = [c for c in range(1, 257)
-             if align256((n_tiles + c) * 32) + align256((c + 2) * 4) + align256(2 * c * 16)
-             + align256(2 * c * 128 * 512 * 4) + align256(2 * c * 128 * 4) == total]
+             if align256((n_tiles + c) * 32) + align256((c + 3) * 4) + align256(2 * c * 16)
+             + align256(c * 16) + align256(2 * c * 128 * 512 * 4) + align256(2 * c * 128 * 4)
+             == total]
     assert len(found) == 1, found
     return found[0]
 
@@ -64,23 +66,26 @@ def run_schedule(prefix, Q, H, causal):
     ncl = clusters_from_size(need, n_tiles)
     raw = ws.cpu().numpy()
     cl_off = align256((n_tiles + ncl) * 32)
-    slot_off = cl_off + align256((ncl + 2) * 4)
-    cl_start = raw[cl_off: cl_off + (ncl + 2) * 4].view(np.int32)
-    n_items, n_slots = int(cl_start[ncl]), int(cl_start[ncl + 1])
+    slot_off = cl_off + align256((ncl + 3) * 4)
+    split_off = slot_off + align256(2 * ncl * 16)
+    cl_start = raw[cl_off: cl_off + (ncl + 3) * 4].view(np.int32)
+    n_items, n_slots, n_split = (int(x) for x in cl_start[ncl:])
     items = raw[: n_items * 32].view(np.int32).reshape(n_items, 8)
     slots = raw[slot_off: slot_off + n_slots * 16].view(np.int32).reshape(n_slots, 4)
-    return dict(ncl=ncl, cl_start=cl_start, items=items, slots=slots, stride=stride,
-                max_prefix=max_prefix, T=T)
+    splits = raw[split_off: split_off + n_split * 16].view(np.int32).reshape(n_split, 4)
+    return dict(ncl=ncl, cl_start=cl_start, items=items, slots=slots, splits=splits,
+                stride=stride, max_prefix=max_prefix, T=T)
 
 
 def check_against_model(prefix, Q, H, causal):
     g = run_schedule(prefix, Q, H, causal)
     ncl = g["ncl"]
-    items, cl_start, slot_info, _ = sched_model.schedule(
+    items, cl_start, slot_info, splits = sched_model.schedule(
         prefix, Q, H, causal, g["max_prefix"], g["stride"], ncl)
     assert g["cl_start"].tolist() == cl_start
     assert g["items"].tolist() == [list(it) for it in items]
     assert g["slots"].tolist() == [list(s) for s in slot_info]
+    assert g["splits"].tolist() == [list(s) for s in splits]
     # every tile's steps swept exactly once, whatever the rules
     swept = {}
     for b, t, s0, s1, *_ in items:

@@ -194,7 +194,8 @@ class HostStepPipeline:
     it has run.  So step i + 1's upload overlaps step i's compute and step i's download,
     and a buffer set is reused only after its previous download has finished.  Every step
     still copies all of its inputs in and its results out.  ``synchronize()`` waits for all
-    submitted steps; results must not be read before it."""
+    submitted steps; results must not be read, nor a step's host inputs changed, before
+    it (the copies run asynchronously from pinned memory)."""
 
     def __init__(self, inp: dict, device="cuda", **step_kw):
         self.device = torch.device(device)

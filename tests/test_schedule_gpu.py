@@ -114,6 +114,9 @@ def prefixes(B, lo, hi, seed):
     (5, 33, 64, 100000, 120000),  # 9 long tiles left over: at most 8 pieces each
     (1100, 1, 64, 0, 500),        # more sequences than are ranked: rounds alternate
     (120, 64, 128, 0, 1000),      # 7680 tiles: 101 rounds, the last 3 dealt by load
+    # 1 to 5 whole rounds around the three dealt ones, ragged prefixes, tiles left over
+    (5, 33, 64, 100, 3000), (9, 33, 64, 100, 3000), (14, 33, 64, 100, 3000),
+    (18, 33, 64, 100, 3000), (23, 33, 64, 100, 3000),
 ])
 def test_tree_schedule_matches_rules(B, Q, H, lo, hi):
     steps = check_against_model(prefixes(B, lo, hi, 40 + B), Q, H, False)

@@ -1,6 +1,6 @@
 """The bf16 parity rule can fail (CPU only, the oracle against variants of itself).
 
-the benchmark spec's bf16 bound, max_abs <= 2e-2, is about as large as the outputs of a softmax
+The stated bf16 bound, max_abs <= 2e-2, is about as large as the outputs of a softmax
 over thousands of keys, so on its own it cannot tell a correct kernel from one that drops
 a term.  tests/compare.py adds a per-row rule derived from the arithmetic (relative rms
 <= 2^-7).  Here the oracle computes two plausible kernel mistakes on two sequences of the
